@@ -1,0 +1,355 @@
+"""Seeded synthetic inputs for chunked-prefill attention over a paged KV cache.
+
+This module only *generates data*: random Q/K/V values, the page permutation, the block
+table, ragged lengths and multimodal ranges, laid out as the library's C ABI expects
+(``include/ppa.h``). It holds none of the attention arithmetic, so both the CUDA path and
+the CPU oracle can take their inputs from it.
+
+Layouts (all row-major, see ``include/ppa.h``):
+
+* ``q``                      ``[total_q, Hq, D]``  bf16
+* ``k_new``, ``v_new``       ``[total_q, Hkv, D]`` bf16
+* ``k_cache``, ``v_cache``   ``[num_pages, P, Hkv, D]`` bf16, or uint8 e4m3fn codes
+* ``block_table``            ``[B, max_pages_per_seq]`` int32 (logical page -> physical page)
+* ``cu_query_lens``          ``[B + 1]`` int32, ``context_lens`` ``[B]`` int32
+* ``mm_ranges``              ``[B, R, 2]`` int32, ``[start, end]`` with ``end`` inclusive
+
+The pages a sequence owns cover all ``c + n`` of its positions (as a serving engine
+allocates them), but only the first ``ceil(c / P)`` are meant to be read. With
+``poison=True`` every cache slot that must never be read (slots of new tokens, spare
+pages, block-table padding) holds NaN, so an implementation that reads one produces NaN
+instead of a silently plausible value.
+
+The named workloads at the bottom follow the shapes of the experiments and tests described
+in the vLLM PR reports on prefix-prefill tiles (PR #54194), windowed key-block skipping
+(PR #50776) and clamped multimodal prefixes (PR #53147); values are N(0, 1), no dataset is
+involved.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class PrefillCase:
+    """One batch of chunked-prefill work, as host (CPU) tensors."""
+
+    name: str
+    seed: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    causal: bool
+    window_left: int
+    window_right: int
+    clamp_mm: bool
+    kv_dtype: str  # "bf16" or "fp8_e4m3"
+    sm_scale: float  # <= 0 means 1/sqrt(head_dim)
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: float
+    v_scale: float
+    block_table: torch.Tensor
+    cu_query_lens: torch.Tensor
+    context_lens: torch.Tensor
+    mm_ranges: Optional[torch.Tensor]
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.numel())
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_query_lens[-1])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_pages_per_seq(self) -> int:
+        return int(self.block_table.shape[1])
+
+    @property
+    def max_mm_ranges(self) -> int:
+        return 0 if self.mm_ranges is None else int(self.mm_ranges.shape[1])
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        cu = self.cu_query_lens.numpy()
+        return (cu[1:] - cu[:-1]).astype(np.int64)
+
+    @property
+    def seq_lens(self) -> np.ndarray:
+        return self.context_lens.numpy().astype(np.int64) + self.query_lens
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name,
+            "seed": self.seed,
+            "num_seqs": self.num_seqs,
+            "total_q": self.total_q,
+            "num_q_heads": self.num_q_heads,
+            "num_kv_heads": self.num_kv_heads,
+            "head_dim": self.head_dim,
+            "page_size": self.page_size,
+            "causal": self.causal,
+            "window_left": self.window_left,
+            "window_right": self.window_right,
+            "mm_ranges_per_seq": self.max_mm_ranges,
+            "clamp_mm": self.clamp_mm,
+            "kv_dtype": self.kv_dtype,
+            "context_tokens": int(self.context_lens.sum()),
+        }
+
+    def numpy_inputs(self) -> dict:
+        """Plain NumPy copies for CPU consumers (bf16 -> float32 is exact)."""
+        out = {
+            "q": self.q.float().numpy(),
+            "k_new": self.k_new.float().numpy(),
+            "v_new": self.v_new.float().numpy(),
+            "block_table": self.block_table.numpy().astype(np.int64),
+            "cu_query_lens": self.cu_query_lens.numpy().astype(np.int64),
+            "context_lens": self.context_lens.numpy().astype(np.int64),
+            "mm_ranges": None if self.mm_ranges is None else self.mm_ranges.numpy().astype(np.int64),
+            "page_size": self.page_size,
+            "num_q_heads": self.num_q_heads,
+            "num_kv_heads": self.num_kv_heads,
+            "head_dim": self.head_dim,
+            "causal": self.causal,
+            "window_left": self.window_left,
+            "window_right": self.window_right,
+            "clamp_mm": self.clamp_mm,
+            "sm_scale": self.sm_scale,
+            "kv_dtype": self.kv_dtype,
+            "k_scale": self.k_scale,
+            "v_scale": self.v_scale,
+        }
+        if self.kv_dtype == "bf16":
+            out["k_cache"] = self.k_cache.float().numpy()
+            out["v_cache"] = self.v_cache.float().numpy()
+        else:
+            out["k_cache"] = self.k_cache.numpy()  # uint8 codes
+            out["v_cache"] = self.v_cache.numpy()
+        return out
+
+
+def _normal_bf16(rng: np.random.Generator, shape) -> torch.Tensor:
+    return torch.from_numpy(rng.standard_normal(size=shape, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _quantize_e4m3(x: torch.Tensor) -> tuple[torch.Tensor, float]:
+    """Per-tensor scale amax/448; codes from torch's round-to-nearest-even cast."""
+    amax = float(x.abs().max()) if x.numel() else 1.0
+    scale = (amax / E4M3_MAX) if amax > 0 else 1.0
+    y = (x.float() / scale).clamp(-E4M3_MAX, E4M3_MAX)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8), float(scale)
+
+
+def build_case(
+    name: str,
+    context_lens: Sequence[int],
+    query_lens: Sequence[int],
+    num_q_heads: int,
+    num_kv_heads: int,
+    head_dim: int,
+    page_size: int,
+    causal: bool = True,
+    window_left: int = 0,
+    window_right: int = 0,
+    mm_ranges: Optional[np.ndarray] = None,
+    clamp_mm: bool = False,
+    kv_dtype: str = "bf16",
+    sm_scale: float = 0.0,
+    seed: int = 0,
+    spare_frac: float = 0.10,
+    poison: bool = True,
+    value_rng_seed: Optional[int] = None,
+) -> PrefillCase:
+    """Build one case. Lengths are per sequence; ``mm_ranges`` is ``[B, R, 2]`` or None."""
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    qlen = np.asarray(query_lens, dtype=np.int64)
+    assert ctx.shape == qlen.shape and ctx.ndim == 1
+    assert (ctx >= 0).all() and (qlen >= 0).all()
+    B = ctx.size
+    P = int(page_size)
+    D = int(head_dim)
+    Hq, Hkv = int(num_q_heads), int(num_kv_heads)
+    rng = np.random.default_rng(seed if value_rng_seed is None else value_rng_seed)
+    layout_rng = np.random.default_rng([seed, 7919])
+
+    total_q = int(qlen.sum())
+    cu = np.zeros(B + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(qlen)
+
+    q = _normal_bf16(rng, (total_q, Hq, D))
+    k_new = _normal_bf16(rng, (total_q, Hkv, D))
+    v_new = _normal_bf16(rng, (total_q, Hkv, D))
+
+    # Pages owned by each sequence cover every position 0..s-1.
+    s = ctx + qlen
+    pages_per_seq = np.array([max(1, math.ceil(int(x) / P)) for x in s], dtype=np.int64)
+    used = int(pages_per_seq.sum())
+    spare = max(1, int(math.ceil(used * spare_frac)))
+    num_pages = used + spare
+    perm = layout_rng.permutation(num_pages)
+    maxp = int(pages_per_seq.max()) if B else 1
+    poison_page = int(perm[used])  # first spare page
+    block_table = np.full((B, maxp), poison_page, dtype=np.int64)
+    off = 0
+    for b in range(B):
+        block_table[b, : pages_per_seq[b]] = perm[off : off + pages_per_seq[b]]
+        off += pages_per_seq[b]
+
+    # Context K/V values, contiguous per sequence, then scattered into their pages.
+    ctx_k = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
+    ctx_v = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
+
+    if kv_dtype == "bf16":
+        fill = float("nan") if poison else 0.0
+        k_cache = torch.full((num_pages, P, Hkv, D), fill, dtype=torch.bfloat16)
+        v_cache = torch.full((num_pages, P, Hkv, D), fill, dtype=torch.bfloat16)
+        k_src, v_src = ctx_k, ctx_v
+        k_scale = v_scale = 1.0
+    elif kv_dtype == "fp8_e4m3":
+        allk = torch.cat(ctx_k) if B else torch.zeros(0)
+        allv = torch.cat(ctx_v) if B else torch.zeros(0)
+        kq, k_scale = _quantize_e4m3(allk)
+        vq, v_scale = _quantize_e4m3(allv)
+        splits = [int(c) for c in ctx]
+        k_src = list(torch.split(kq, splits)) if B else []
+        v_src = list(torch.split(vq, splits)) if B else []
+        fill = 0x7F if poison else 0
+        k_cache = torch.full((num_pages, P, Hkv, D), fill, dtype=torch.uint8)
+        v_cache = torch.full((num_pages, P, Hkv, D), fill, dtype=torch.uint8)
+    else:
+        raise ValueError(f"unknown kv_dtype {kv_dtype!r}")
+
+    for b in range(B):
+        c = int(ctx[b])
+        for lp in range(math.ceil(c / P)):
+            lo, hi = lp * P, min(c, (lp + 1) * P)
+            phys = int(block_table[b, lp])
+            k_cache[phys, : hi - lo] = k_src[b][lo:hi]
+            v_cache[phys, : hi - lo] = v_src[b][lo:hi]
+
+    mm = None
+    if mm_ranges is not None:
+        mm = torch.from_numpy(np.asarray(mm_ranges, dtype=np.int32).reshape(B, -1, 2).copy())
+
+    return PrefillCase(
+        name=name,
+        seed=seed,
+        num_q_heads=Hq,
+        num_kv_heads=Hkv,
+        head_dim=D,
+        page_size=P,
+        causal=bool(causal),
+        window_left=int(window_left),
+        window_right=int(window_right),
+        clamp_mm=bool(clamp_mm),
+        kv_dtype=kv_dtype,
+        sm_scale=float(sm_scale),
+        q=q,
+        k_new=k_new,
+        v_new=v_new,
+        k_cache=k_cache,
+        v_cache=v_cache,
+        k_scale=float(k_scale),
+        v_scale=float(v_scale),
+        block_table=torch.from_numpy(block_table.astype(np.int32)),
+        cu_query_lens=torch.from_numpy(cu.astype(np.int32)),
+        context_lens=torch.from_numpy(ctx.astype(np.int32)),
+        mm_ranges=mm,
+    )
+
+
+# ---------------------------------------------------------------------------------------
+# The named workloads. Each takes a ``scale`` in (0, 1] that shrinks lengths for parity
+# tests the CPU oracle finishes in seconds while keeping the structure.
+# ---------------------------------------------------------------------------------------
+
+NONPOW2_SHAPES = [  # (num_q_heads, q heads per kv head, head_dim, page_size)
+    (64, 1, 128, 544),
+    (8, 4, 256, 1040),
+    (8, 4, 256, 1056),
+]
+
+MIXED_PAGE_SIZES = [128, 512, 544, 1040, 1056, 2048]
+
+
+def _scaled(x: int, scale: float, lo: int = 1) -> int:
+    return max(lo, int(round(x * scale)))
+
+
+def tiny(seed: int = 0, **kw) -> PrefillCase:
+    """Batch 2, 4 q heads / 2 kv heads, D 64, page 16, context [0, 37], queries [19, 8], causal."""
+    return build_case("tiny", [0, 37], [19, 8], 4, 2, 64, 16, causal=True, seed=seed, **kw)
+
+
+def nonpow2(shape_idx: int, seed: int = 0, scale: float = 1.0, num_seqs: int = 8, **kw) -> PrefillCase:
+    """Ragged batch, context U[0, 8192], query U[1, 2048], causal, non-power-of-2 pages."""
+    hq, g, d, p = NONPOW2_SHAPES[shape_idx]
+    rng = np.random.default_rng([seed, 101, shape_idx])
+    ctx = rng.integers(0, _scaled(8192, scale, 0) + 1, size=num_seqs)
+    qlen = rng.integers(1, _scaled(2048, scale) + 1, size=num_seqs)
+    return build_case(f"nonpow2_h{hq}_g{g}_d{d}_p{p}", ctx, qlen, hq, hq // g, d, p,
+                      causal=True, seed=seed, **kw)
+
+
+def swa_noncausal(seed: int = 0, scale: float = 1.0, **kw) -> PrefillCase:
+    """One sequence of 16384 new tokens, 8 heads, D 64, window 64 both sides, non-causal."""
+    n = _scaled(16384, scale)
+    return build_case("swa64_noncausal", [0], [n], 8, 8, 64, 16, causal=False,
+                      window_left=64, window_right=64, seed=seed, **kw)
+
+
+def swa_causal(seed: int = 0, scale: float = 1.0, seq_len: int = 32768, window: int = 1024,
+               **kw) -> PrefillCase:
+    """One sequence of 32768 new tokens, 8 heads, D 64, causal, left window 1024."""
+    n = _scaled(seq_len, scale)
+    return build_case(f"swa{window}_causal_{seq_len}", [0], [n], 8, 8, 64, 16, causal=True,
+                      window_left=window, seed=seed, **kw)
+
+
+def mm_ranges_for(seq_len: int, num_ranges: int, width: int, rng: np.random.Generator) -> np.ndarray:
+    """Non-overlapping ranges [a, a + width - 1] at seeded random starts."""
+    free = seq_len - num_ranges * width
+    assert free >= 0
+    u = np.sort(rng.integers(0, free + 1, size=num_ranges))
+    a = u + width * np.arange(num_ranges)
+    return np.stack([a, a + width - 1], axis=-1)
+
+
+def clamped_mm(seed: int = 0, scale: float = 1.0, num_seqs: int = 4, num_ranges: int = 60,
+               range_width: int = 256, **kw) -> PrefillCase:
+    """4 x 16384 tokens, 16 q / 8 kv heads, D 256, causal, window 1024, 60 clamped ranges."""
+    n = _scaled(16384, scale)
+    rng = np.random.default_rng([seed, 303])
+    nr = min(num_ranges, n // range_width)
+    ranges = np.stack([mm_ranges_for(n, nr, range_width, rng) for _ in range(num_seqs)])
+    return build_case("clamped_mm", [0] * num_seqs, [n] * num_seqs, 16, 8, 256, 16, causal=True,
+                      window_left=_scaled(1024, scale), mm_ranges=ranges, clamp_mm=True,
+                      seed=seed, **kw)
+
+
+def mixed(page_size: int, windowed: bool, kv_dtype: str = "bf16", seed: int = 0,
+          scale: float = 1.0, num_seqs: int = 32, **kw) -> PrefillCase:
+    """32 seqs, context U[4096, 32768], query U[512, 4096], 32 q / 4 kv heads, D 128, causal."""
+    rng = np.random.default_rng([seed, 505])
+    ctx = rng.integers(_scaled(4096, scale, 0), _scaled(32768, scale, 0) + 1, size=num_seqs)
+    qlen = rng.integers(_scaled(512, scale), _scaled(4096, scale) + 1, size=num_seqs)
+    wl = _scaled(4096, scale) if windowed else 0
+    return build_case(f"mixed_p{page_size}_w{wl}_{kv_dtype}", ctx, qlen, 32, 4, 128, page_size,
+                      causal=True, window_left=wl, kv_dtype=kv_dtype, seed=seed, **kw)
