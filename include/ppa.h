@@ -1,0 +1,155 @@
+/*
+ * ppa.h -- chunked-prefill attention over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * One batch of sequences is processed per call. Sequence b has c = context_lens[b] cached
+ * tokens and n = cu_query_lens[b+1] - cu_query_lens[b] new query tokens, so s = c + n keys.
+ * Query token j of sequence b sits at absolute position q = c + j. Key positions p < c are
+ * read from the paged cache through the block table, one token at a time: physical page
+ * block_table[b][p / P], slot p % P. Key positions p >= c are read from k_new / v_new.
+ * Tiles of keys may therefore straddle page boundaries, and P may be any positive integer.
+ * Sources: vLLM PR #54194 report (prefix-prefill tiles decoupled from the page size),
+ * sections "功能与动机" and "关键源码片段" (context_attention_fwd, _paged_kv_cache_offsets).
+ *
+ * Mask: a query at q may attend to key k (0 <= k < s) iff base(q,k) OR mm(q,k).
+ *   base: (causal ? k <= q : (window_right <= 0 || k - q < window_right))
+ *         && (window_left <= 0 || q - k < window_left)
+ *   mm:   some range [a, e] of the sequence with a < e has a <= q <= e' and a <= k <= e',
+ *         with e' = min(e, s - 1), and, when PPA_FLAG_CLAMP_MM is set and window_left > 0,
+ *         also q - k < window_left.
+ * Sources: "[Kernel][Gemma4] Prune Triton sliding-window tiles for multimodal prefixes"
+ * (PR #53147), sections "实现拆解" 1-2 and "关键源码片段" (compute_tile_loop_bounds); and
+ * "[Kernel] Skip fully masked key blocks in windowed Triton prefill" (PR #50776), section
+ * "关键源码片段" (separate left/right windows, 0 = off).
+ *
+ * Output: out[q, h] = sum_k softmax_k(sm_scale * <Q[q,h], K[k, h/G]>) V[k, h/G] over the
+ * allowed keys, where G = num_q_heads / num_kv_heads (query heads g*G .. g*G+G-1 share KV
+ * head g; PR #53147 "关键源码片段", BLOCK_M = BLOCK_Q * num_queries_per_kv).
+ * Key tiles that hold no allowed pair are never loaded (PR #50776 "功能与动机"; PR #53147
+ * "实现拆解" 2): a first stage computes the exact interval of live key tiles per query tile.
+ *
+ * Tensor layouts (row-major, element offsets in elements of the stated type):
+ *   q            [total_q][num_q_heads][head_dim]            bf16
+ *   k_new, v_new [total_q][num_kv_heads][head_dim]           bf16
+ *   k_cache,
+ *   v_cache      [num_pages][page_size][num_kv_heads][head_dim]  bf16 or fp8 e4m3fn (1 byte)
+ *   block_table  [num_seqs][max_pages_per_seq]                int32, physical page ids
+ *   cu_query_lens[num_seqs + 1]                              int32, cu[0] = 0, cu[B] = total_q
+ *   context_lens [num_seqs]                                  int32, >= 0
+ *   mm_ranges    [num_seqs][max_mm_ranges][2]                int32 {start, end}, end inclusive;
+ *                                                            entries with start >= end are unused
+ *   out          [total_q][num_q_heads][head_dim]            bf16
+ * Only the first ceil(c / P) entries of a block-table row are ever read.
+ *
+ * Ownership and synchronisation: every pointer is a device pointer owned by the caller.
+ * The library allocates nothing, never frees, never synchronises inside ppa_prefill, and
+ * runs all work on `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ * Argument errors found on the host return a status at once and launch nothing. Errors found
+ * on the device (bad lengths, a page id outside [0, num_pages), an expired bounded wait) are
+ * written to the caller's int32 `device_status` (first error wins). The kernels then skip
+ * the affected work instead of faulting; ppa_read_status() reports the code.
+ */
+#ifndef PPA_H_
+#define PPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PPA_OK = 0,
+  PPA_ERR_INVALID = 1,     /* bad argument (host) or bad lengths found on the device */
+  PPA_ERR_UNSUPPORTED = 2, /* head_dim / group size / dtype / path with no kernel in this build */
+  PPA_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy, attribute) */
+  PPA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired; the kernel returned early */
+  PPA_ERR_BAD_PAGE = 5     /* a block-table entry outside [0, num_pages); rows read as zero */
+} ppa_status;
+
+enum { PPA_KV_BF16 = 0, PPA_KV_FP8_E4M3 = 1 };
+
+enum {
+  PPA_FLAG_CAUSAL = 1u,   /* base mask is causal (k <= q); window_right is then ignored */
+  PPA_FLAG_CLAMP_MM = 2u, /* multimodal keys also obey the left window (q - k < window_left) */
+  PPA_FLAG_NO_PRUNE = 4u  /* testing: visit every key tile 0 .. ceil(s/TN)-1 and mask them */
+};
+
+typedef struct {
+  int num_seqs;          /* B >= 0 */
+  int total_q;           /* sum of query lengths, >= 0 */
+  int num_q_heads;       /* Hq >= 1 */
+  int num_kv_heads;      /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 128 */
+  int head_dim;          /* D: 64, 128 or 256 */
+  int page_size;         /* P >= 1, any integer */
+  int num_pages;         /* physical pages in each cache tensor, >= 1 */
+  int max_pages_per_seq; /* block-table row length, >= 1 */
+  int max_mm_ranges;     /* R >= 0; mm_ranges may be NULL when 0 */
+  int window_left;       /* <= 0: unbounded on the left */
+  int window_right;      /* <= 0: unbounded on the right (ignored when causal) */
+  int kv_dtype;          /* PPA_KV_BF16 or PPA_KV_FP8_E4M3 */
+  unsigned flags;        /* PPA_FLAG_* */
+  float sm_scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+} ppa_dims;
+
+/* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list).
+ * Returns 0 if dims is NULL or invalid. The caller allocates it; contents need no
+ * initialisation and may be reused across calls on the same stream. */
+size_t ppa_workspace_bytes(const ppa_dims* dims);
+
+/* The attention forward pass. Pointers as in the layout table above; k_scale / v_scale are
+ * device pointers to one fp32 each (the per-tensor dequantisation scales), required when
+ * kv_dtype is PPA_KV_FP8_E4M3 and ignored otherwise. k_new / v_new must be non-NULL (a
+ * cache-sourced path without them returns PPA_ERR_UNSUPPORTED). q, k_new, v_new, k_cache,
+ * v_cache and out must be 16-byte aligned. Launches two stages on `stream`: the live-tile
+ * bounds and work list, then the persistent attention kernel. */
+ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* cu_query_lens, const int32_t* context_lens,
+                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                       void* out, void* workspace, int32_t* device_status, void* stream);
+
+/* The tile shape ppa_prefill uses for `dims`: tq query tokens per query tile (so tq * G <= 128
+ * rows) and tn keys per key tile. Writes 0 to both if dims is invalid. */
+void ppa_query_tiles(const ppa_dims* dims, int* tq, int* tn);
+
+/* Stage 1 alone, for testing: for every (sequence, query tile of tq tokens) in order, writes
+ * {lo, hi} (int32 pairs) such that key tiles lo .. hi-1 of width tn are exactly those holding
+ * an allowed pair (PR #53147 "关键源码片段", compute_tile_loop_bounds; we use the first query
+ * row for the window edge). bounds_out must hold 2 * sum_b ceil(n_b / tq) ints. */
+ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* cu_query_lens,
+                           const int32_t* context_lens, const int32_t* mm_ranges,
+                           int32_t* bounds_out, int32_t* device_status, void* stream);
+
+/* Testing: the allowed-pair bitmap of sequence `seq` as the attention kernel evaluates it:
+ * bit (k % 32) of word bitmap[j * words_per_row + k / 32] is set iff query token j may attend
+ * to key k. Rows j < min(n, max_rows) are written, words beyond ceil(s/32) are zeroed. */
+ppa_status ppa_debug_mask(const ppa_dims* dims, int seq, const int32_t* cu_query_lens,
+                          const int32_t* context_lens, const int32_t* mm_ranges,
+                          uint32_t* bitmap_out, int max_rows, int words_per_row, void* stream);
+
+/* Number of allowed (query token, key) pairs summed over the batch, for one head; written
+ * to the device uint64 *count_out. Live-pair FLOPs are 4 * D * Hq * count. */
+ppa_status ppa_live_pairs(const ppa_dims* dims, const int32_t* cu_query_lens,
+                          const int32_t* context_lens, const int32_t* mm_ranges,
+                          unsigned long long* count_out, void* stream);
+
+/* Testing: decodes n fp8 e4m3fn codes to bf16 bit patterns with the attention kernel's own
+ * conversion (exact; NaN codes give a bf16 NaN). */
+ppa_status ppa_debug_e4m3_to_bf16(const uint8_t* codes, uint16_t* bf16_out, int n, void* stream);
+
+/* Synchronises `stream`, returns the code stored in *device_status and clears it to 0.
+ * Returns PPA_ERR_CUDA if the synchronisation or the copy fails. */
+ppa_status ppa_read_status(int32_t* device_status, void* stream);
+
+/* Static text for a status code. */
+const char* ppa_status_string(ppa_status status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int ppa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PPA_H_ */

@@ -1,0 +1,273 @@
+// The C ABI declared in include/ppa.h: argument validation, workspace sizing and the two
+// launches of ppa_prefill. Nothing here allocates, frees or synchronises, except
+// ppa_read_status, whose job is to synchronise.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/ppa.h"
+#include "ppa_internal.cuh"
+#include "ppa_kernels.h"
+
+namespace {
+
+using ppa::QTile;
+using ppa::WsHeader;
+
+constexpr unsigned kKnownFlags = PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ppa_status check_dims(const ppa_dims* d) {
+  if (d == nullptr) return PPA_ERR_INVALID;
+  if (d->num_seqs < 0 || d->total_q < 0) return PPA_ERR_INVALID;
+  if (d->num_q_heads < 1 || d->num_kv_heads < 1) return PPA_ERR_INVALID;
+  if (d->num_q_heads % d->num_kv_heads != 0) return PPA_ERR_INVALID;
+  if (d->page_size < 1 || d->num_pages < 1 || d->max_pages_per_seq < 1) return PPA_ERR_INVALID;
+  if (d->max_mm_ranges < 0) return PPA_ERR_INVALID;
+  if ((d->flags & ~kKnownFlags) != 0u) return PPA_ERR_INVALID;
+  if (!std::isfinite(d->sm_scale)) return PPA_ERR_INVALID;
+  if (d->kv_dtype != PPA_KV_BF16 && d->kv_dtype != PPA_KV_FP8_E4M3) return PPA_ERR_INVALID;
+  if (d->num_q_heads / d->num_kv_heads > ppa::kRowsPerTile) return PPA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return PPA_ERR_UNSUPPORTED;
+  // element offsets are formed in 64-bit; rows and tokens must fit int32
+  if ((long long)d->num_pages * d->page_size > INT_MAX) return PPA_ERR_INVALID;
+  if ((long long)d->total_q * d->num_q_heads > INT_MAX) return PPA_ERR_INVALID;
+  return PPA_OK;
+}
+
+int group_of(const ppa_dims* d) { return d->num_q_heads / d->num_kv_heads; }
+
+long long max_qtiles_for(const ppa_dims* d, int tq) {
+  return ((long long)d->total_q + tq - 1) / tq + d->num_seqs;
+}
+
+ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
+  ppa::MaskParams m;
+  m.causal = (d->flags & PPA_FLAG_CAUSAL) ? 1 : 0;
+  m.window_left = d->window_left;
+  m.window_right = d->window_right;
+  m.clamp_mm = (d->flags & PPA_FLAG_CLAMP_MM) ? 1 : 0;
+  m.max_mm_ranges = (mm_ranges != nullptr) ? d->max_mm_ranges : 0;
+  m.mm_ranges = (d->max_mm_ranges > 0) ? mm_ranges : nullptr;
+  return m;
+}
+
+struct WsLayout {
+  size_t header, qtiles, order, total;
+};
+
+WsLayout ws_layout(const ppa_dims* d) {
+  const long long mq = max_qtiles_for(d, ppa::tokens_per_qtile(group_of(d)));
+  WsLayout w;
+  w.header = 0;
+  w.qtiles = align_up(sizeof(WsHeader), 256);
+  w.order = align_up(w.qtiles + (size_t)mq * sizeof(QTile), 256);
+  w.total = align_up(w.order + (size_t)mq * sizeof(int32_t), 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ppa_workspace_bytes(const ppa_dims* dims) {
+  if (check_dims(dims) != PPA_OK) return 0;
+  return ws_layout(dims).total;
+}
+
+void ppa_query_tiles(const ppa_dims* dims, int* tq, int* tn) {
+  const bool ok = check_dims(dims) == PPA_OK;
+  if (tq) *tq = ok ? ppa::tokens_per_qtile(group_of(dims)) : 0;
+  if (tn) *tn = ok ? ppa::keys_per_tile(dims->head_dim) : 0;
+}
+
+ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* cu_query_lens, const int32_t* context_lens,
+                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                       void* out, void* workspace, int32_t* device_status, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return PPA_ERR_UNSUPPORTED;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      cu_query_lens == nullptr || context_lens == nullptr || out == nullptr ||
+      workspace == nullptr || device_status == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  const bool fp8 = dims->kv_dtype == PPA_KV_FP8_E4M3;
+  if (fp8 && (k_scale == nullptr || v_scale == nullptr)) return PPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+    return PPA_ERR_INVALID;
+  if (dims->num_seqs == 0 || dims->total_q == 0) return PPA_OK;  // nothing to compute
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = group_of(dims);
+  const int tq = ppa::tokens_per_qtile(G);
+  const int tn = ppa::keys_per_tile(dims->head_dim);
+  const long long mq = max_qtiles_for(dims, tq);
+  if (mq * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
+  const WsLayout w = ws_layout(dims);
+  char* ws = static_cast<char*>(workspace);
+
+  ppa::Stage1Params s1{};
+  s1.num_seqs = dims->num_seqs;
+  s1.total_q = dims->total_q;
+  s1.tq = tq;
+  s1.tn = tn;
+  s1.num_kv_heads = dims->num_kv_heads;
+  s1.page_size = dims->page_size;
+  s1.max_pages_per_seq = dims->max_pages_per_seq;
+  s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
+  s1.max_qtiles = (int)mq;
+  s1.mask = mask_of(dims, mm_ranges);
+  s1.cu_query_lens = cu_query_lens;
+  s1.context_lens = context_lens;
+  s1.ws = reinterpret_cast<WsHeader*>(ws + w.header);
+  s1.qtiles = reinterpret_cast<QTile*>(ws + w.qtiles);
+  s1.order = reinterpret_cast<int32_t*>(ws + w.order);
+  s1.bounds_out = nullptr;
+  s1.status = device_status;
+  if (ppa::launch_stage1(s1, true, s) != cudaSuccess) return PPA_ERR_CUDA;
+
+  ppa::AttnParams a{};
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.cu_query_lens = cu_query_lens;
+  a.context_lens = context_lens;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.out = out;
+  a.ws = s1.ws;
+  a.qtiles = s1.qtiles;
+  a.order = s1.order;
+  a.status = device_status;
+  a.mask = s1.mask;
+  a.num_q_heads = dims->num_q_heads;
+  a.num_kv_heads = dims->num_kv_heads;
+  a.group = G;
+  a.tq = tq;
+  a.page_size = dims->page_size;
+  a.num_pages = dims->num_pages;
+  a.max_pages_per_seq = dims->max_pages_per_seq;
+  const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);
+  a.scale_log2 = sm * 1.4426950408889634f;
+  const int max_items = (int)(mq * dims->num_kv_heads);
+  cudaError_t e;
+  switch (dims->head_dim) {
+    case 64: e = ppa::launch_attn_d64(a, fp8, max_items, s); break;
+    case 128: e = ppa::launch_attn_d128(a, fp8, max_items, s); break;
+    default: e = ppa::launch_attn_d256(a, fp8, max_items, s); break;
+  }
+  return e == cudaSuccess ? PPA_OK : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* cu_query_lens,
+                           const int32_t* context_lens, const int32_t* mm_ranges,
+                           int32_t* bounds_out, int32_t* device_status, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (tq < 1 || tn < 1 || cu_query_lens == nullptr || context_lens == nullptr ||
+      bounds_out == nullptr || device_status == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  if (dims->num_seqs == 0) return PPA_OK;
+  ppa::Stage1Params s1{};
+  s1.num_seqs = dims->num_seqs;
+  s1.total_q = dims->total_q;
+  s1.tq = tq;
+  s1.tn = tn;
+  s1.num_kv_heads = dims->num_kv_heads;
+  s1.page_size = dims->page_size;
+  s1.max_pages_per_seq = dims->max_pages_per_seq;
+  s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
+  const long long mq = max_qtiles_for(dims, tq);
+  if (mq > INT_MAX / 2) return PPA_ERR_INVALID;
+  s1.max_qtiles = (int)mq;
+  s1.mask = mask_of(dims, mm_ranges);
+  s1.cu_query_lens = cu_query_lens;
+  s1.context_lens = context_lens;
+  s1.bounds_out = bounds_out;
+  s1.status = device_status;
+  return ppa::launch_stage1(s1, false, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_debug_mask(const ppa_dims* dims, int seq, const int32_t* cu_query_lens,
+                          const int32_t* context_lens, const int32_t* mm_ranges,
+                          uint32_t* bitmap_out, int max_rows, int words_per_row, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (seq < 0 || seq >= dims->num_seqs || max_rows < 0 || words_per_row < 1 ||
+      cu_query_lens == nullptr || context_lens == nullptr || bitmap_out == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  if (max_rows == 0) return PPA_OK;
+  return ppa::launch_debug_mask(mask_of(dims, mm_ranges), seq, cu_query_lens, context_lens,
+                                bitmap_out, max_rows, words_per_row,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_live_pairs(const ppa_dims* dims, const int32_t* cu_query_lens,
+                          const int32_t* context_lens, const int32_t* mm_ranges,
+                          unsigned long long* count_out, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (cu_query_lens == nullptr || context_lens == nullptr || count_out == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  return ppa::launch_live_pairs(mask_of(dims, mm_ranges), dims->num_seqs, dims->total_q,
+                                cu_query_lens, context_lens, count_out,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_debug_e4m3_to_bf16(const uint8_t* codes, uint16_t* bf16_out, int n, void* stream) {
+  if (n < 0 || (n > 0 && (codes == nullptr || bf16_out == nullptr))) return PPA_ERR_INVALID;
+  return ppa::launch_e4m3_decode(codes, bf16_out, n, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_read_status(int32_t* device_status, void* stream) {
+  if (device_status == nullptr) return PPA_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t code = 0;
+  if (cudaMemcpyAsync(&code, device_status, sizeof(code), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return PPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PPA_ERR_CUDA;
+  if (cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess) return PPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PPA_ERR_CUDA;
+  return static_cast<ppa_status>(code);
+}
+
+const char* ppa_status_string(ppa_status status) {
+  switch (status) {
+    case PPA_OK: return "ok";
+    case PPA_ERR_INVALID: return "invalid argument";
+    case PPA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PPA_ERR_CUDA: return "CUDA runtime error";
+    case PPA_ERR_TIMEOUT: return "device-side wait timed out";
+    case PPA_ERR_BAD_PAGE: return "block-table entry out of range";
+  }
+  return "unknown status";
+}
+
+int ppa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// Shared device-side definitions: launch parameters, the workspace layout, status
+// reporting and the mask arithmetic that both the tile-bounds stage and the attention
+// kernel evaluate (so the two can never disagree).
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/ppa.h"
+
+namespace ppa {
+
+constexpr int kRowsPerTile = 128;  // rows of one query tile (tokens x heads of a group)
+
+// Mask parameters of one call.
+struct MaskParams {
+  int causal;
+  int window_left;   // <= 0: off
+  int window_right;  // <= 0: off (ignored when causal)
+  int clamp_mm;
+  int max_mm_ranges;
+  const int32_t* mm_ranges;  // [B][R][2] or nullptr
+};
+
+// Workspace header; followed by the query-tile table and the work list.
+struct WsHeader {
+  int32_t next_item;  // work-stealing counter of the persistent kernel
+  int32_t n_items;    // number of (query tile, kv head) items, 0 on a device-side error
+  int32_t n_qtiles;
+  int32_t pad[13];
+};
+
+// One query tile: sequence, tile index within the sequence, live key tiles [lo, hi).
+struct QTile {
+  int32_t seq, t, lo, hi;
+};
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Allowed keys of one query position q form the single interval [kmin, kmax], which always
+// contains q: the base window contains q, every multimodal range that contains q contains q,
+// and the union of intervals that share a point is an interval.
+//   base: [WL > 0 ? q - WL + 1 : 0,  causal ? q : (WR > 0 ? q + WR - 1 : s - 1)]
+//   mm:   for each valid range [a, e'] containing q: [clamp && WL > 0 ? max(a, q - WL + 1) : a, e']
+// ("[Kernel][Gemma4] Prune Triton sliding-window tiles for multimodal prefixes", 实现拆解 2:
+// the multimodal mask is OR-ed onto the base mask, so bounds take the union.)
+__device__ __forceinline__ void row_interval(int q, int s, const MaskParams& mp,
+                                             const int32_t* ranges /* this sequence, [R][2] */,
+                                             int& kmin, int& kmax) {
+  int lo = mp.window_left > 0 ? q - mp.window_left + 1 : 0;
+  int hi;
+  if (mp.causal) {
+    hi = q;
+  } else if (mp.window_right > 0) {
+    hi = (mp.window_right - 1 >= s - 1 - q) ? s - 1 : q + mp.window_right - 1;
+  } else {
+    hi = s - 1;
+  }
+  if (ranges != nullptr) {
+    const bool clamp = mp.clamp_mm && mp.window_left > 0;
+    for (int r = 0; r < mp.max_mm_ranges; ++r) {
+      const int a = ranges[2 * r];
+      const int e = ranges[2 * r + 1];
+      if (!(a < e)) continue;
+      const int e2 = e < s - 1 ? e : s - 1;
+      if (a <= q && q <= e2) {
+        const int l = clamp ? max(a, q - mp.window_left + 1) : a;
+        lo = min(lo, l);
+        hi = max(hi, e2);
+      }
+    }
+  }
+  kmin = max(lo, 0);
+  kmax = hi;
+}
+
+// Union of the row intervals of query positions q_lo .. q_hi (one query tile), in closed
+// form. A range contributes iff it shares a row with the tile; its lowest key over those rows
+// is max(a, q_lo - WL + 1) when clamped (the window edge of the tile's first row), else a.
+// The base lower edge also uses the first row, q_lo (the page computes it from the last row,
+// which is not a bound for the earlier rows of the block).
+__device__ __forceinline__ void tile_interval(int q_lo, int q_hi, int s, const MaskParams& mp,
+                                              const int32_t* ranges, int& klo, int& khi) {
+  int lo = mp.window_left > 0 ? q_lo - mp.window_left + 1 : 0;
+  int hi;
+  if (mp.causal) {
+    hi = q_hi;
+  } else if (mp.window_right > 0) {
+    hi = (mp.window_right - 1 >= s - 1 - q_hi) ? s - 1 : q_hi + mp.window_right - 1;
+  } else {
+    hi = s - 1;
+  }
+  if (ranges != nullptr) {
+    const bool clamp = mp.clamp_mm && mp.window_left > 0;
+    for (int r = 0; r < mp.max_mm_ranges; ++r) {
+      const int a = ranges[2 * r];
+      const int e = ranges[2 * r + 1];
+      if (!(a < e)) continue;
+      const int e2 = e < s - 1 ? e : s - 1;
+      if (a <= q_hi && e2 >= q_lo) {
+        const int l = clamp ? max(a, q_lo - mp.window_left + 1) : a;
+        lo = min(lo, l);
+        hi = max(hi, e2);
+      }
+    }
+  }
+  klo = max(lo, 0);
+  khi = hi;
+}
+
+// Tile shape for a head group of G query heads: tq tokens x G heads <= 128 rows.
+__host__ __device__ inline int tokens_per_qtile(int group) { return kRowsPerTile / group; }
+__host__ __device__ inline int keys_per_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+
+}  // namespace ppa

@@ -1,0 +1,61 @@
+// Launch parameters and launchers shared between the C-ABI layer (ppa_api.cu) and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ppa_internal.cuh"
+
+namespace ppa {
+
+struct Stage1Params {
+  int num_seqs, total_q, tq, tn, num_kv_heads, page_size, max_pages_per_seq, no_prune;
+  int max_qtiles;
+  MaskParams mask;
+  const int32_t* cu_query_lens;
+  const int32_t* context_lens;
+  WsHeader* ws;         // work-list mode
+  QTile* qtiles;        // work-list mode: [max_qtiles]
+  int32_t* order;       // work-list mode: [max_qtiles], query tiles heaviest first
+  int32_t* bounds_out;  // bounds-only mode: [max_qtiles][2]
+  int32_t* status;
+};
+
+struct AttnParams {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* cu_query_lens;
+  const int32_t* context_lens;
+  const float* k_scale;  // fp8 only
+  const float* v_scale;  // fp8 only
+  void* out;
+  WsHeader* ws;
+  const QTile* qtiles;
+  const int32_t* order;
+  int32_t* status;
+  MaskParams mask;
+  int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+cudaError_t launch_stage1(const Stage1Params& p, bool worklist, cudaStream_t stream);
+cudaError_t launch_debug_mask(const MaskParams& mp, int seq, const int32_t* cu, const int32_t* ctx,
+                              uint32_t* bitmap, int max_rows, int words_per_row,
+                              cudaStream_t stream);
+cudaError_t launch_live_pairs(const MaskParams& mp, int num_seqs, int total_q, const int32_t* cu,
+                              const int32_t* ctx, unsigned long long* out, cudaStream_t stream);
+cudaError_t launch_e4m3_decode(const uint8_t* codes, uint16_t* out, int n, cudaStream_t stream);
+
+// Attention kernels, one translation unit per head dimension. `max_ctas` bounds the
+// persistent grid (the number of work items cannot be known on the host).
+cudaError_t launch_attn_d64(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
+cudaError_t launch_attn_d128(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
+cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
+
+}  // namespace ppa

@@ -1,0 +1,129 @@
+"""Attention output of the CUDA path against the CPU oracle (bf16 out, atol = rtol = 2e-2),
+on seeded inputs small enough for the oracle, spanning several tiles and ragged tails, plus
+the invariances the method guarantees."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ref
+from paged_kv_prefix_gb300 import binding
+from paged_kv_prefix_gb300 import workloads as wl
+from tests.gpu_util import assert_close, parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_config():
+    err, _ = parity(wl.tiny(seed=0))
+    assert err < 2e-2
+
+
+@pytest.mark.parametrize("shape", [0, 1, 2])
+def test_nonpow2_pages_scaled(shape):
+    parity(wl.nonpow2(shape, seed=1, scale=1 / 8))
+
+
+def test_swa_noncausal_scaled():
+    parity(wl.swa_noncausal(seed=2, scale=1 / 16))
+
+
+def test_swa_causal_scaled():
+    parity(wl.swa_causal(seed=3, seq_len=2048, window=256))
+
+
+def test_clamped_mm_scaled():
+    parity(wl.clamped_mm(seed=4, scale=1 / 16, num_ranges=3))
+
+
+@pytest.mark.parametrize("page", [128, 544, 1056])
+@pytest.mark.parametrize("windowed", [False, True])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_mixed_scaled(page, windowed, kv):
+    parity(wl.mixed(page, windowed, kv_dtype=kv, seed=5, scale=1 / 16, num_seqs=6))
+
+
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("group", [1, 3, 8])
+@pytest.mark.parametrize("page", [1, 5, 16, 37])
+def test_ragged_geometry(head_dim, group, page):
+    """Odd page sizes (tiles straddle many pages), empty and one-token sequences, contexts
+    that end mid-page, GQA groups that do not divide 128."""
+    rng = np.random.default_rng(head_dim * 100 + group * 10 + page)
+    ctx = [0, 1, 37, int(rng.integers(100, 400)), 0, 130]
+    qlen = [1, 0, 19, int(rng.integers(130, 300)), 200, 3]
+    parity(wl.build_case("ragged", ctx, qlen, 2 * group, 2, head_dim, page, causal=True,
+                         window_left=int(rng.choice([0, 50])), seed=page))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_windows_and_ranges_combined(causal):
+    rng = np.random.default_rng(7)
+    mm = np.array([[[10, 90], [150, 400], [0, 0]], [[0, 500], [3, 2], [600, 700]]])
+    parity(wl.build_case("combo", [60, 300], [400, 420], 8, 2, 128, 16, causal=causal,
+                         window_left=70, window_right=33, mm_ranges=mm, clamp_mm=True,
+                         seed=int(rng.integers(1 << 30))))
+    parity(wl.build_case("combo_unclamped", [60, 300], [400, 420], 8, 2, 128, 16, causal=causal,
+                         window_left=70, window_right=33, mm_ranges=mm, clamp_mm=False, seed=8))
+
+
+def test_fp8_kv_scaled():
+    parity(wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=9, scale=1 / 16, num_seqs=4))
+
+
+def test_page_permutation_is_bitwise_invariant():
+    a = wl.build_case("perm", [300, 1000], [200, 333], 8, 2, 128, 544, causal=True, seed=10,
+                      value_rng_seed=77)
+    b = wl.build_case("perm", [300, 1000], [200, 333], 8, 2, 128, 544, causal=True, seed=11,
+                      value_rng_seed=77)
+    assert not torch.equal(a.block_table, b.block_table)
+    oa = run_gpu(a).out.cpu()
+    ob = run_gpu(b).out.cpu()
+    assert torch.equal(oa, ob)
+
+
+@pytest.mark.parametrize("factory", [
+    lambda: wl.swa_noncausal(seed=12, scale=1 / 32),
+    lambda: wl.clamped_mm(seed=13, scale=1 / 32, num_ranges=2),
+    lambda: wl.mixed(1040, True, seed=14, scale=1 / 16, num_seqs=3),
+])
+def test_pruned_equals_unpruned_bitwise(factory):
+    case = factory()
+    pruned = run_gpu(case).out.cpu()
+    full = run_gpu(case, flags_extra=binding.PPA_FLAG_NO_PRUNE).out.cpu()
+    assert torch.equal(pruned.float(), full.float())
+
+
+def test_removing_a_range_changes_gpu_output():
+    case = wl.clamped_mm(seed=15, scale=1 / 16, num_seqs=1, num_ranges=2, range_width=100)
+    with_mm = run_gpu(case).out.float().cpu().numpy()
+    a, e = case.mm_ranges[0, 0].tolist()
+    case.mm_ranges[0, 0] = torch.tensor([0, 0], dtype=torch.int32)
+    without = run_gpu(case).out.float().cpu().numpy()
+    assert np.abs(with_mm[a:e - 1] - without[a:e - 1]).max() > 2e-2
+    assert_close(without, ref.attention(case.numpy_inputs()), "without range")
+
+
+def test_single_allowed_key_returns_value_row():
+    case = wl.build_case("one", [0, 40], [150, 70], 4, 2, 64, 16, causal=True, window_left=1,
+                         seed=16)
+    got = run_gpu(case).out.float().cpu()
+    want = case.v_new.float().repeat_interleave(2, dim=1)
+    assert torch.equal(got, want)
+
+
+def test_status_reports_bad_page_without_faulting():
+    case = wl.build_case("badpage", [40], [10], 2, 1, 64, 16, causal=True, seed=17)
+    case.block_table[0, 1] = case.num_pages + 5
+    dc = binding.DeviceCase(case)
+    dc.run()
+    torch.cuda.synchronize()
+    assert dc.read_status() == binding.PPA_ERR_BAD_PAGE
+
+
+def test_status_reports_bad_lengths():
+    case = wl.tiny(seed=0)
+    dc = binding.DeviceCase(case)
+    dc.cu_query_lens[1] = -5
+    dc.run()
+    torch.cuda.synchronize()
+    assert dc.read_status() == binding.PPA_ERR_INVALID

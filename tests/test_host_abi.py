@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every entry
+point include/ppa.h declares, sizes its workspace and rejects invalid arguments before
+launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_prefix_gb300 import binding
+from paged_kv_prefix_gb300 import workloads as wl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ppa.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ppa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.lib()
+    names = _declared_functions()
+    assert "ppa_prefill" in names and len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(binding._SIGNATURES)
+
+
+def test_status_strings_and_version():
+    assert binding.ppa_status_string(0) == "ok"
+    assert "timed out" in binding.ppa_status_string(binding.PPA_ERR_TIMEOUT)
+    assert binding.ppa_status_string(99) == "unknown status"
+    assert binding.ppa_version() >= 100
+
+
+def _dims(**kw):
+    d = binding.dims_for(wl.tiny())
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_tiles_and_workspace():
+    d = _dims()
+    assert binding.ppa_query_tiles(d) == (64, 128)  # G = 2 -> 64 tokens x 2 heads
+    assert binding.ppa_workspace_bytes(d) > 0
+    assert binding.ppa_query_tiles(_dims(num_q_heads=32, num_kv_heads=4, head_dim=256)) == (16, 64)
+    assert binding.ppa_query_tiles(_dims(num_q_heads=6, num_kv_heads=2)) == (42, 128)
+    assert binding.ppa_workspace_bytes(_dims(head_dim=96)) == 0
+    assert binding.ppa_query_tiles(_dims(head_dim=96)) == (0, 0)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, binding.PPA_ERR_UNSUPPORTED),
+    ("num_kv_heads", 3, binding.PPA_ERR_INVALID),
+    ("num_q_heads", 0, binding.PPA_ERR_INVALID),
+    ("page_size", 0, binding.PPA_ERR_INVALID),
+    ("num_pages", 0, binding.PPA_ERR_INVALID),
+    ("num_seqs", -1, binding.PPA_ERR_INVALID),
+    ("kv_dtype", 7, binding.PPA_ERR_INVALID),
+    ("flags", 64, binding.PPA_ERR_INVALID),
+    ("sm_scale", float("nan"), binding.PPA_ERR_INVALID),
+    ("max_mm_ranges", -2, binding.PPA_ERR_INVALID),
+])
+def test_invalid_dims_rejected(field, value, code):
+    d = _dims(**{field: value})
+    fake = 1 << 20  # never dereferenced: validation fails first
+    got = binding.ppa_prefill(d, fake, fake, fake, fake, fake, fake, fake, fake, None, None, None,
+                              fake, fake, fake, stream=0, check=False)
+    assert got == code
+
+
+def test_null_and_misaligned_pointers_rejected():
+    d = _dims()
+    f = 1 << 20
+    args = [f] * 8 + [None, None, None, f, f, f]  # never launched: each call below is rejected
+    # cache-sourced path (k_new = NULL) is not available
+    a = list(args)
+    a[1] = None
+    assert binding.ppa_prefill(d, *a, stream=0, check=False) == binding.PPA_ERR_UNSUPPORTED
+    # missing output
+    a = list(args)
+    a[11] = None
+    assert binding.ppa_prefill(d, *a, stream=0, check=False) == binding.PPA_ERR_INVALID
+    # misaligned q
+    a = list(args)
+    a[0] = f + 2
+    assert binding.ppa_prefill(d, *a, stream=0, check=False) == binding.PPA_ERR_INVALID
+    # multimodal ranges declared but not passed
+    d2 = _dims(max_mm_ranges=3)
+    assert binding.ppa_prefill(d2, *args, stream=0, check=False) == binding.PPA_ERR_INVALID
+    # fp8 without scales
+    d3 = _dims(kv_dtype=binding.PPA_KV_FP8_E4M3)
+    assert binding.ppa_prefill(d3, *args, stream=0, check=False) == binding.PPA_ERR_INVALID
+
+
+def test_empty_batch_launches_nothing():
+    d = _dims(num_seqs=0, total_q=0)
+    f = 1 << 20
+    assert binding.ppa_prefill(d, *([f] * 8), None, None, None, f, f, f, stream=0,
+                               check=False) == binding.PPA_OK
+
+
+def test_test_entry_points_validate():
+    d = _dims()
+    f = 1 << 20
+    assert binding.ppa_tile_bounds(d, 0, 32, f, f, None, f, f, stream=0, check=False) == 1
+    assert binding.ppa_debug_mask(d, 5, f, f, None, f, 1, 1, stream=0, check=False) == 1
+    assert binding.ppa_debug_e4m3_to_bf16(None, None, -1, stream=0, check=False) == 1
+    assert binding.ppa_read_status(None, stream=0) == 1
+    assert binding.ppa_live_pairs(d, None, f, None, f, stream=0, check=False) == 1
