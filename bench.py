@@ -1,0 +1,466 @@
+"""Benchmark: chunked-prefill attention over a paged KV cache on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload nonpow2|swa64|swa1024|mm|mixed] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path over one batch: for every shape of the workload,
+stage 1 (live key-tile bounds and work list) and the attention kernel, through the C ABI.
+The default workload is the non-power-of-2-pages batch: 8 ragged sequences (context
+U[0, 8192], query U[1, 2048], causal) for each of the head shapes (64 q heads, G 1, D 128,
+page 544), (8, G 4, D 256, page 1040) and (8, G 4, D 256, page 1056). Values are seeded N(0,1)
+(synthetic data). L2 (129 MB) is flushed between timed steps by writing 512 MiB; the flush is
+outside the timed region.
+
+Prints one JSON line (rank 0). ``value`` is TFLOP/s over live (query, key) pairs:
+4 * D * Hq per pair, pairs counted by the library's own interval arithmetic.
+Under torchrun each rank runs its own seeded batch (weak scaling, no data-path collective);
+the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s (live pairs) & % GB300 bf16 TC peak; tokens/s at 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------------------
+def make_workload(name: str, seed: int):
+    from paged_kv_prefix_gb300 import workloads as wl
+    if name == "nonpow2":
+        return ("non-power-of-2 pages: 8 seqs, ctx U[0,8192], q U[1,2048], causal; "
+                "(Hq,G,D,P) = (64,1,128,544), (8,4,256,1040), (8,4,256,1056)",
+                [wl.nonpow2(i, seed=seed) for i in range(3)])
+    if name == "swa64":
+        return ("sliding window 64/64 non-causal, 1 seq x 16384, 8 heads, D 64, page 16",
+                [wl.swa_noncausal(seed=seed)])
+    if name == "swa1024":
+        return ("sliding window 1024 causal, 1 seq x 32768, 8 heads, D 64, page 16",
+                [wl.swa_causal(seed=seed)])
+    if name == "mm":
+        return ("clamped multimodal: 4 seqs x 16384, 16 q / 8 kv heads, D 256, page 16, causal, "
+                "window 1024, 60 ranges x 256 tokens", [wl.clamped_mm(seed=seed)])
+    if name == "mixed":
+        return ("mixed serving: 32 seqs, ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, "
+                "D 128, causal, page 544, no window, bf16 KV", [wl.mixed(544, False, seed=seed)])
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_prefix_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu capture, if it still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle baseline (the only place bench.py runs oracle/)
+# ---------------------------------------------------------------------------------------
+def oracle_sample(cases, budget_s: float, rng_seed: int = 0):
+    """Times the oracle on evenly spaced query tokens of each case until ~budget_s of CPU
+    work. Returns (live-pair FLOPs computed, seconds, description)."""
+    from oracle import ref
+    flops, secs, tokens = 0.0, 0.0, 0
+    per_case = budget_s / len(cases)
+    for case in cases:
+        inp = case.numpy_inputs()
+        cu = inp["cu_query_lens"]
+        B = case.num_seqs
+        b = int(np.argmax([(cu[i + 1] - cu[i]) * (inp["context_lens"][i] + cu[i + 1] - cu[i])
+                           for i in range(B)]))
+        c = int(inp["context_lens"][b])
+        n = int(cu[b + 1] - cu[b])
+        kv = (ref.gather_kv(inp, b, "k"), ref.gather_kv(inp, b, "v"))
+        spent, count = 0.0, 2
+        while spent < per_case and count <= n:
+            toks = np.linspace(0, n - 1, num=min(count, n)).astype(np.int64)
+            t0 = time.perf_counter()
+            ref.attention_rows(inp, b, toks, kv=kv)
+            dt = time.perf_counter() - t0
+            pairs = int(ref.allowed_mask(c + toks, c + n, case.causal, case.window_left,
+                                         case.window_right, None if inp["mm_ranges"] is None
+                                         else inp["mm_ranges"][b], case.clamp_mm).sum())
+            flops += 4.0 * case.head_dim * case.num_q_heads * pairs
+            secs += dt
+            tokens += len(toks)
+            spent += dt
+            count *= 2
+    return flops, secs, f"{tokens} query tokens (all heads) of the heaviest sequence of each shape"
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------------------
+def run_reference(args):
+    dist, rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    desc, cases = make_workload(args.workload, seed=0)
+    per_step = args.ref_step_seconds
+    for _ in range(args.warmup):
+        oracle_sample(cases, per_step / 4)
+    total_f, total_s, sample = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, s, sample = oracle_sample(cases, per_step)
+        total_f += f
+        total_s += s
+    tflops = total_f / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    from paged_kv_prefix_gb300 import binding
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.lib()
+    desc, cases = make_workload(args.workload, seed=rank)
+    dcs = [binding.DeviceCase(c, device=dev) for c in cases]
+    stream = torch.cuda.current_stream(dev)
+
+    # live pairs and FLOPs, from the library's interval arithmetic
+    flops, tokens = [], 0
+    for dc, case in zip(dcs, cases):
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        binding.ppa_live_pairs(dc.dims, dc.cu_query_lens, dc.context_lens, dc.mm_ranges, cnt,
+                               stream)
+        flops.append(4.0 * case.head_dim * case.num_q_heads * float(cnt.item()))
+        tokens += case.total_q
+    step_flops = sum(flops)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step(ev_list):
+        for i, dc in enumerate(dcs):
+            ev_list[i][0].record(stream)
+            dc.plan(stream)
+            ev_list[i][1].record(stream)
+            dc.attend(stream)
+            ev_list[i][2].record(stream)
+
+    mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in dcs]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+    for dc in dcs:
+        st = dc.read_status(stream)
+        if st != 0:
+            raise SystemExit(f"device status {st}: {binding.status_string(st)}")
+
+    events = [mk() for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(events[k])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = [sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(len(dcs))) for ev in events]
+    attend_ms = np.array([[ev[i][1].elapsed_time(ev[i][2]) for i in range(len(dcs))]
+                          for ev in events])  # [steps, shapes]
+    plan_ms = np.array([[ev[i][0].elapsed_time(ev[i][1]) for i in range(len(dcs))]
+                        for ev in events])
+    total_ms = max_over_ranks(dist, float(sum(step_ms)), dev)
+    all_flops = sum_over_ranks(dist, step_flops * args.steps, dev)
+    all_tokens = sum_over_ranks(dist, float(tokens * args.steps), dev)
+    for dc in dcs:
+        st = dc.read_status(stream)
+        if st != 0:
+            raise SystemExit(f"device status {st}: {binding.status_string(st)}")
+
+    # ---- e2e: host buffers in, host result out, through the same public API ----
+    e2e = run_e2e(args, cases, dcs, step_flops, stream, dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    value = all_flops / (total_ms * 1e-3) / 1e12
+    # dominant kernel: the attention launch with the largest total time
+    shape_tot = attend_ms.sum(axis=0)
+    dom = int(np.argmax(shape_tot))
+    dom_avg_s = float(attend_ms[:, dom].mean()) * 1e-3
+    achieved = flops[dom] / dom_avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    shapes = []
+    for i, case in enumerate(cases):
+        a = float(attend_ms[:, i].mean())
+        shapes.append({"shape": case.name, "attend_ms": round(a, 4),
+                       "plan_ms": round(float(plan_ms[:, i].mean()), 4),
+                       "tflops": round(flops[i] / (a * 1e-3) / 1e12, 2),
+                       "live_tflop": round(flops[i] / 1e12, 4)})
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        f, s, sample = oracle_sample(cases, args.cpu_seconds)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample + f" ({s:.1f} s)"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc, "l2": "flushed between timed steps (512 MiB write)",
+                   "seed_per_rank": "rank"},
+        "pct_bf16_peak": 100.0 * value / peak,
+        "tokens_per_s": all_tokens / (total_ms * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+                     "kernel": f"attn_kernel ({cases[dom].name})",
+                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "shapes": shapes,
+        "e2e": e2e,
+        "gpu_launches": 2 * len(dcs) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, cases, dcs, step_flops, stream, dev):
+    """Same metric with host inputs: per step, pinned-host -> device copies of every input,
+    the C-ABI call, and a device -> host copy of the output, all inside the timed region."""
+    import torch
+    from paged_kv_prefix_gb300 import binding
+
+    names = ["q", "k_new", "v_new", "k_cache", "v_cache", "block_table", "cu_query_lens",
+             "context_lens"]
+    host = []
+    h2d = d2h = 0
+    for case, dc in zip(cases, dcs):
+        hs = {n: getattr(case, n).pin_memory() for n in names}
+        if case.mm_ranges is not None:
+            hs["mm_ranges"] = case.mm_ranges.pin_memory()
+        hs["k_scale"] = torch.tensor([case.k_scale], dtype=torch.float32).pin_memory()
+        hs["v_scale"] = torch.tensor([case.v_scale], dtype=torch.float32).pin_memory()
+        hs["out"] = torch.empty_like(case.q).pin_memory()
+        h2d += sum(v.numel() * v.element_size() for k, v in hs.items() if k != "out")
+        d2h += hs["out"].numel() * hs["out"].element_size()
+        host.append(hs)
+
+    def one():
+        for hs, dc in zip(host, dcs):
+            for n in names:
+                getattr(dc, n).copy_(hs[n], non_blocking=True)
+            if dc.mm_ranges is not None:
+                dc.mm_ranges.copy_(hs["mm_ranges"], non_blocking=True)
+            dc.k_scale.copy_(hs["k_scale"], non_blocking=True)
+            dc.v_scale.copy_(hs["v_scale"], non_blocking=True)
+            dc.run(stream)
+            hs["out"].copy_(dc.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="nonpow2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

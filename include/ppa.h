@@ -101,13 +101,34 @@ size_t ppa_workspace_bytes(const ppa_dims* dims);
  * device pointers to one fp32 each (the per-tensor dequantisation scales), required when
  * kv_dtype is PPA_KV_FP8_E4M3 and ignored otherwise. k_new / v_new must be non-NULL (a
  * cache-sourced path without them returns PPA_ERR_UNSUPPORTED). q, k_new, v_new, k_cache,
- * v_cache and out must be 16-byte aligned. Launches two stages on `stream`: the live-tile
- * bounds and work list, then the persistent attention kernel. */
+ * v_cache and out must be 16-byte aligned. Launches two stages on `stream`: ppa_plan (the
+ * live-tile bounds and work list) and ppa_attend (the persistent attention kernel). */
 ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
                        const void* k_cache, const void* v_cache, const int32_t* block_table,
                        const int32_t* cu_query_lens, const int32_t* context_lens,
                        const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
                        void* out, void* workspace, int32_t* device_status, void* stream);
+
+/* The two stages of ppa_prefill, callable separately so that one plan serves every layer of
+ * a batch (the lengths, ranges and mask parameters do not change between layers).
+ *
+ * ppa_plan (stage 1): validates the lengths on the device, computes every query tile's
+ * live key-tile interval and the work list (heaviest tiles first) into `workspace`.
+ *
+ * ppa_attend (stage 2): the attention kernel over the work list in `workspace`. The
+ * workspace must hold a plan made by ppa_plan for the same dims and the same
+ * cu_query_lens / context_lens / mm_ranges contents; the plan is left intact, so any number
+ * of ppa_attend calls may follow one ppa_plan on the same stream. Calls that share a
+ * workspace must not overlap in time (they share its work-stealing counter). */
+ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
+                    const int32_t* context_lens, const int32_t* mm_ranges, void* workspace,
+                    int32_t* device_status, void* stream);
+
+ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                      const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      const int32_t* cu_query_lens, const int32_t* context_lens,
+                      const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                      void* out, void* workspace, int32_t* device_status, void* stream);
 
 /* The tile shape ppa_prefill uses for `dims`: tq query tokens per query tile (so tq * G <= 128
  * rows) and tn keys per key tile. Writes 0 to both if dims is invalid. */

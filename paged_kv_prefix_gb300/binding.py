@@ -62,6 +62,8 @@ _DIMS = ctypes.POINTER(PpaDims)
 _SIGNATURES = {
     "ppa_workspace_bytes": (ctypes.c_size_t, [_DIMS]),
     "ppa_prefill": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ppa_plan": (_I, [_DIMS, _P, _P, _P, _P, _P, _P]),
+    "ppa_attend": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ppa_query_tiles": (None, [_DIMS, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "ppa_tile_bounds": (_I, [_DIMS, _I, _I, _P, _P, _P, _P, _P, _P]),
     "ppa_debug_mask": (_I, [_DIMS, _I, _P, _P, _P, _P, _I, _I, _P]),
@@ -139,6 +141,28 @@ def ppa_prefill(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table, c
                              _ptr(device_status), _stream(stream))
     if check:
         _check(code, "ppa_prefill")
+    return code
+
+
+def ppa_plan(dims: PpaDims, cu_query_lens, context_lens, mm_ranges, workspace, device_status,
+             stream=None, check: bool = True) -> int:
+    code = lib().ppa_plan(ctypes.byref(dims), _ptr(cu_query_lens), _ptr(context_lens),
+                          _ptr(mm_ranges), _ptr(workspace), _ptr(device_status), _stream(stream))
+    if check:
+        _check(code, "ppa_plan")
+    return code
+
+
+def ppa_attend(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
+               context_lens, mm_ranges, k_scale, v_scale, out, workspace, device_status,
+               stream=None, check: bool = True) -> int:
+    code = lib().ppa_attend(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new),
+                            _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                            _ptr(cu_query_lens), _ptr(context_lens), _ptr(mm_ranges),
+                            _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(workspace),
+                            _ptr(device_status), _stream(stream))
+    if check:
+        _check(code, "ppa_attend")
     return code
 
 
@@ -235,6 +259,16 @@ class DeviceCase:
                            self.block_table, self.cu_query_lens, self.context_lens,
                            self.mm_ranges, self.k_scale, self.v_scale,
                            self.out if out is None else out, self.workspace, self.status, stream)
+
+    def plan(self, stream=None):
+        return ppa_plan(self.dims, self.cu_query_lens, self.context_lens, self.mm_ranges,
+                        self.workspace, self.status, stream)
+
+    def attend(self, stream=None, out=None):
+        return ppa_attend(self.dims, self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                          self.block_table, self.cu_query_lens, self.context_lens,
+                          self.mm_ranges, self.k_scale, self.v_scale,
+                          self.out if out is None else out, self.workspace, self.status, stream)
 
     def read_status(self, stream=None) -> int:
         return ppa_read_status(self.status, stream)

@@ -86,11 +86,50 @@ void ppa_query_tiles(const ppa_dims* dims, int* tq, int* tn) {
   if (tn) *tn = ok ? ppa::keys_per_tile(dims->head_dim) : 0;
 }
 
-ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
-                       const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       const int32_t* cu_query_lens, const int32_t* context_lens,
-                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
-                       void* out, void* workspace, int32_t* device_status, void* stream) {
+ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
+                    const int32_t* context_lens, const int32_t* mm_ranges, void* workspace,
+                    int32_t* device_status, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (cu_query_lens == nullptr || context_lens == nullptr || workspace == nullptr ||
+      device_status == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  if (!aligned16(workspace)) return PPA_ERR_INVALID;
+  if (dims->num_seqs == 0 || dims->total_q == 0) return PPA_OK;  // nothing to plan
+  const int tq = ppa::tokens_per_qtile(group_of(dims));
+  const long long mq = max_qtiles_for(dims, tq);
+  if (mq * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
+  const WsLayout w = ws_layout(dims);
+  char* ws = static_cast<char*>(workspace);
+  ppa::Stage1Params s1{};
+  s1.num_seqs = dims->num_seqs;
+  s1.total_q = dims->total_q;
+  s1.tq = tq;
+  s1.tn = ppa::keys_per_tile(dims->head_dim);
+  s1.num_kv_heads = dims->num_kv_heads;
+  s1.page_size = dims->page_size;
+  s1.max_pages_per_seq = dims->max_pages_per_seq;
+  s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
+  s1.max_qtiles = (int)mq;
+  s1.mask = mask_of(dims, mm_ranges);
+  s1.cu_query_lens = cu_query_lens;
+  s1.context_lens = context_lens;
+  s1.ws = reinterpret_cast<WsHeader*>(ws + w.header);
+  s1.qtiles = reinterpret_cast<QTile*>(ws + w.qtiles);
+  s1.order = reinterpret_cast<int32_t*>(ws + w.order);
+  s1.bounds_out = nullptr;
+  s1.status = device_status;
+  return ppa::launch_stage1(s1, true, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                      const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      const int32_t* cu_query_lens, const int32_t* context_lens,
+                      const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                      void* out, void* workspace, int32_t* device_status, void* stream) {
   const ppa_status st = check_dims(dims);
   if (st != PPA_OK) return st;
   if (k_new == nullptr || v_new == nullptr) return PPA_ERR_UNSUPPORTED;
@@ -106,34 +145,12 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
     return PPA_ERR_INVALID;
   if (dims->num_seqs == 0 || dims->total_q == 0) return PPA_OK;  // nothing to compute
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = group_of(dims);
   const int tq = ppa::tokens_per_qtile(G);
-  const int tn = ppa::keys_per_tile(dims->head_dim);
   const long long mq = max_qtiles_for(dims, tq);
   if (mq * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
   const WsLayout w = ws_layout(dims);
   char* ws = static_cast<char*>(workspace);
-
-  ppa::Stage1Params s1{};
-  s1.num_seqs = dims->num_seqs;
-  s1.total_q = dims->total_q;
-  s1.tq = tq;
-  s1.tn = tn;
-  s1.num_kv_heads = dims->num_kv_heads;
-  s1.page_size = dims->page_size;
-  s1.max_pages_per_seq = dims->max_pages_per_seq;
-  s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
-  s1.max_qtiles = (int)mq;
-  s1.mask = mask_of(dims, mm_ranges);
-  s1.cu_query_lens = cu_query_lens;
-  s1.context_lens = context_lens;
-  s1.ws = reinterpret_cast<WsHeader*>(ws + w.header);
-  s1.qtiles = reinterpret_cast<QTile*>(ws + w.qtiles);
-  s1.order = reinterpret_cast<int32_t*>(ws + w.order);
-  s1.bounds_out = nullptr;
-  s1.status = device_status;
-  if (ppa::launch_stage1(s1, true, s) != cudaSuccess) return PPA_ERR_CUDA;
 
   ppa::AttnParams a{};
   a.q = q;
@@ -147,11 +164,11 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.out = out;
-  a.ws = s1.ws;
-  a.qtiles = s1.qtiles;
-  a.order = s1.order;
+  a.ws = reinterpret_cast<WsHeader*>(ws + w.header);
+  a.qtiles = reinterpret_cast<const QTile*>(ws + w.qtiles);
+  a.order = reinterpret_cast<const int32_t*>(ws + w.order);
   a.status = device_status;
-  a.mask = s1.mask;
+  a.mask = mask_of(dims, mm_ranges);
   a.num_q_heads = dims->num_q_heads;
   a.num_kv_heads = dims->num_kv_heads;
   a.group = G;
@@ -162,6 +179,7 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
   const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);
   a.scale_log2 = sm * 1.4426950408889634f;
   const int max_items = (int)(mq * dims->num_kv_heads);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (dims->head_dim) {
     case 64: e = ppa::launch_attn_d64(a, fp8, max_items, s); break;
@@ -169,6 +187,31 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
     default: e = ppa::launch_attn_d256(a, fp8, max_items, s); break;
   }
   return e == cudaSuccess ? PPA_OK : PPA_ERR_CUDA;
+}
+
+ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* cu_query_lens, const int32_t* context_lens,
+                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                       void* out, void* workspace, int32_t* device_status, void* stream) {
+  // Validate everything ppa_attend checks before ppa_plan launches anything.
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return PPA_ERR_UNSUPPORTED;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      out == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->kv_dtype == PPA_KV_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr))
+    return PPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out))
+    return PPA_ERR_INVALID;
+  const ppa_status sp = ppa_plan(dims, cu_query_lens, context_lens, mm_ranges, workspace,
+                                 device_status, stream);
+  if (sp != PPA_OK) return sp;
+  return ppa_attend(dims, q, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
+                    context_lens, mm_ranges, k_scale, v_scale, out, workspace, device_status,
+                    stream);
 }
 
 ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* cu_query_lens,

@@ -46,7 +46,7 @@ struct AttnCfg {
   static constexpr int KV_OFF = Q_OFF + Q_BYTES;          // stage s: K at +2s*KV, V at +(2s+1)*KV
   static constexpr int P_OFF = KV_OFF + 4 * KV_BYTES;     // two stages of K and V
   static constexpr int MISC_OFF = P_OFF + P_BYTES;
-  static constexpr int MISC_BYTES = 64 + 2 * TN * 8;      // barriers, slots, row pointers
+  static constexpr int MISC_BYTES = 64 + 4 * TN * 8;      // barriers, slots, row pointers x2
   static constexpr int SMEM_BYTES = MISC_OFF + MISC_BYTES + 1024;  // + alignment slack
   static constexpr int TMEM_S = 0;
   static constexpr int TMEM_O = TN;
@@ -154,8 +154,9 @@ __global__ void __launch_bounds__(128, 1) attn_kernel(const AttnParams p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 24);
   int* s_item = reinterpret_cast<int*>(misc + 28);
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 32);
-  const char** rowK = reinterpret_cast<const char**>(misc + 64);
-  const char** rowV = rowK + C::TN;
+  // Row-pointer tables, one per K/V stage: the gather of tile kt+1 fills its table while
+  // threads may still be reading tile kt's.
+  const char** rowK0 = reinterpret_cast<const char**>(misc + 64);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(128, 1) attn_kernel(const AttnParams p) {
     const int lo = qt.lo, hi = qt.hi;
     if (lo < hi) {
       gather_kv_tile<D, FP8>(p, b, g, c, s, q_start, lo * C::TN, base + C::KV_OFF,
-                             base + C::KV_OFF + C::KV_BYTES, rowK, rowV);
+                             base + C::KV_OFF + C::KV_BYTES, rowK0, rowK0 + C::TN);
     }
     cp_async_commit();
 
@@ -238,8 +239,9 @@ __global__ void __launch_bounds__(128, 1) attn_kernel(const AttnParams p) {
       const uint32_t sV = sK + C::KV_BYTES;
       if (kt + 1 < hi) {
         const uint32_t nK = base + C::KV_OFF + (2 * (st ^ 1)) * C::KV_BYTES;
+        const char** rk = rowK0 + 2 * C::TN * (st ^ 1);
         gather_kv_tile<D, FP8>(p, b, g, c, s, q_start, (kt + 1) * C::TN, nK, nK + C::KV_BYTES,
-                               rowK, rowV);
+                               rk, rk + C::TN);
       }
       cp_async_commit();
       cp_async_wait<1>();
@@ -384,6 +386,16 @@ __global__ void __launch_bounds__(128, 1) attn_kernel(const AttnParams p) {
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  // The last CTA to finish re-arms the work counter, so the plan in the workspace can serve
+  // the next launch on the stream without another stage-1 pass.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&p.ws->done_ctas, 1) == (int)gridDim.x - 1) {
+      p.ws->next_item = 0;
+      p.ws->done_ctas = 0;
+      __threadfence();
+    }
   }
 }
 

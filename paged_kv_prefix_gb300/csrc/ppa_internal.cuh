@@ -23,10 +23,11 @@ struct MaskParams {
 
 // Workspace header; followed by the query-tile table and the work list.
 struct WsHeader {
-  int32_t next_item;  // work-stealing counter of the persistent kernel
-  int32_t n_items;    // number of (query tile, kv head) items, 0 on a device-side error
+  int32_t next_item;   // work-stealing counter of the persistent kernel
+  int32_t n_items;     // number of (query tile, kv head) items, 0 on a device-side error
   int32_t n_qtiles;
-  int32_t pad[13];
+  int32_t done_ctas;   // CTAs of the running attention launch that have finished
+  int32_t pad[12];
 };
 
 // One query tile: sequence, tile index within the sequence, live key tiles [lo, hi).

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kStage1Threads) stage1_kernel(const Stage1Para
       p.ws->n_items = 0;
       p.ws->n_qtiles = 0;
       p.ws->next_item = 0;
+      p.ws->done_ctas = 0;
     }
     return;
   }
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kStage1Threads) stage1_kernel(const Stage1Para
     p.ws->n_qtiles = n_qtiles;
     p.ws->n_items = n_qtiles * p.num_kv_heads;
     p.ws->next_item = 0;
+    p.ws->done_ctas = 0;
   }
 }
 
