@@ -130,6 +130,33 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
                       void* out, void* workspace, int32_t* device_status, void* stream);
 
+/* Size of the scratch ppa_prefill_noalloc keeps in a static device array: 2 MiB, enough for
+ * about 100,000 query tiles (20 bytes each, plus under 1 KiB of header and padding). */
+#define PPA_NOALLOC_WORKSPACE_BYTES (2u << 20)
+
+/* ppa_prefill for callers that cannot allocate device memory: no workspace argument.
+ * The paged-attention pages have no counterpart of this entry point; it exists for callers
+ * such as a plugin inside a host framework that owns the whole device memory pool and gives
+ * its plugins no allocator, or a runtime that forbids device allocation after start-up to
+ * keep a fixed memory footprint. The scratch ppa_prefill would take from `workspace` lives
+ * instead in one file-scope device array of PPA_NOALLOC_WORKSPACE_BYTES, which every GPU that
+ * loads the library holds until the process exits. This call allocates and frees nothing.
+ *   - Inputs, `out` and `device_status` are the caller's, exactly as for ppa_prefill.
+ *   - A batch whose ppa_workspace_bytes() exceeds PPA_NOALLOC_WORKSPACE_BYTES is rejected
+ *     with PPA_ERR_UNSUPPORTED before anything is launched (use ppa_prefill for it).
+ *   - The first call on each device looks up that device's address of the array (with the
+ *     device current) and caches it; make that first call before any stream capture.
+ *   - All calls on a device share the one array. Calls whose work overlaps on the GPU (other
+ *     streams, other host threads without ordering) race on it and give wrong results; calls
+ *     ordered on one stream are safe. Each call rewrites every scratch word it reads, so
+ *     leftovers of the previous call need no clearing. */
+ppa_status ppa_prefill_noalloc(const ppa_dims* dims, const void* q, const void* k_new,
+                               const void* v_new, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, const int32_t* cu_query_lens,
+                               const int32_t* context_lens, const int32_t* mm_ranges,
+                               const float* k_scale, const float* v_scale, void* out,
+                               int32_t* device_status, void* stream);
+
 /* The tile shape ppa_prefill uses for `dims`: tq query tokens per query tile (so tq * G <= 128
  * rows) and tn keys per key tile. Writes 0 to both if dims is invalid. */
 void ppa_query_tiles(const ppa_dims* dims, int* tq, int* tn);

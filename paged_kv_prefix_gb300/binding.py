@@ -64,6 +64,8 @@ _SIGNATURES = {
     "ppa_prefill": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ppa_plan": (_I, [_DIMS, _P, _P, _P, _P, _P, _P]),
     "ppa_attend": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ppa_prefill_noalloc": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _P]),
     "ppa_query_tiles": (None, [_DIMS, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "ppa_tile_bounds": (_I, [_DIMS, _I, _I, _P, _P, _P, _P, _P, _P]),
     "ppa_debug_mask": (_I, [_DIMS, _I, _P, _P, _P, _P, _I, _I, _P]),
@@ -141,6 +143,25 @@ def ppa_prefill(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table, c
                              _ptr(device_status), _stream(stream))
     if check:
         _check(code, "ppa_prefill")
+    return code
+
+
+PPA_NOALLOC_WORKSPACE_BYTES = 2 << 20
+
+
+def ppa_prefill_noalloc(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table,
+                        cu_query_lens, context_lens, mm_ranges, k_scale, v_scale, out,
+                        device_status, stream=None, check: bool = True) -> int:
+    """ppa_prefill without a workspace argument, for callers that cannot allocate device
+    memory; the scratch lives in the library's static device array (shared by all calls on
+    a device, so calls must not overlap on the GPU)."""
+    code = lib().ppa_prefill_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                     _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                     _ptr(cu_query_lens), _ptr(context_lens), _ptr(mm_ranges),
+                                     _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                     _ptr(device_status), _stream(stream))
+    if check:
+        _check(code, "ppa_prefill_noalloc")
     return code
 
 
