@@ -13,7 +13,6 @@
 
 namespace {
 
-using ppa::QTile;
 using ppa::WsHeader;
 
 constexpr unsigned kKnownFlags = PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE;
@@ -58,16 +57,21 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
 }
 
 struct WsLayout {
-  size_t header, qtiles, order, total;
+  size_t header, seq_unit_base, seq_cost, seq_order, seq_item_base, units, items, total;
 };
 
 WsLayout ws_layout(const ppa_dims* d) {
   const long long mq = max_qtiles_for(d, ppa::tokens_per_qtile(group_of(d)));
+  const size_t seq_ints = (size_t)d->num_seqs + 1;
   WsLayout w;
   w.header = 0;
-  w.qtiles = align_up(sizeof(WsHeader), 256);
-  w.order = align_up(w.qtiles + (size_t)mq * sizeof(QTile), 256);
-  w.total = align_up(w.order + (size_t)mq * sizeof(int32_t), 256);
+  w.seq_unit_base = align_up(sizeof(WsHeader), 256);
+  w.seq_cost = align_up(w.seq_unit_base + seq_ints * 4, 256);
+  w.seq_order = align_up(w.seq_cost + seq_ints * 4, 256);
+  w.seq_item_base = align_up(w.seq_order + seq_ints * 4, 256);
+  w.units = align_up(w.seq_item_base + seq_ints * 4, 256);
+  w.items = align_up(w.units + (size_t)mq * sizeof(ppa::Unit), 256);
+  w.total = align_up(w.items + (size_t)mq * d->num_kv_heads * 4, 256);
   return w;
 }
 
@@ -112,15 +116,20 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   s1.max_pages_per_seq = dims->max_pages_per_seq;
   s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
   s1.max_qtiles = (int)mq;
+  s1.nq = ppa::tiles_per_unit(dims->head_dim);
   s1.mask = mask_of(dims, mm_ranges);
   s1.cu_query_lens = cu_query_lens;
   s1.context_lens = context_lens;
   s1.ws = reinterpret_cast<WsHeader*>(ws + w.header);
-  s1.qtiles = reinterpret_cast<QTile*>(ws + w.qtiles);
-  s1.order = reinterpret_cast<int32_t*>(ws + w.order);
+  s1.seq_unit_base = reinterpret_cast<int32_t*>(ws + w.seq_unit_base);
+  s1.seq_cost = reinterpret_cast<int32_t*>(ws + w.seq_cost);
+  s1.seq_order = reinterpret_cast<int32_t*>(ws + w.seq_order);
+  s1.seq_item_base = reinterpret_cast<int32_t*>(ws + w.seq_item_base);
+  s1.units = reinterpret_cast<ppa::Unit*>(ws + w.units);
+  s1.items = reinterpret_cast<int32_t*>(ws + w.items);
   s1.bounds_out = nullptr;
   s1.status = device_status;
-  return ppa::launch_stage1(s1, true, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return ppa::launch_plan(s1, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PPA_OK
              : PPA_ERR_CUDA;
 }
@@ -165,8 +174,8 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.v_scale = v_scale;
   a.out = out;
   a.ws = reinterpret_cast<WsHeader*>(ws + w.header);
-  a.qtiles = reinterpret_cast<const QTile*>(ws + w.qtiles);
-  a.order = reinterpret_cast<const int32_t*>(ws + w.order);
+  a.units = reinterpret_cast<const ppa::Unit*>(ws + w.units);
+  a.items = reinterpret_cast<const int32_t*>(ws + w.items);
   a.status = device_status;
   a.mask = mask_of(dims, mm_ranges);
   a.num_q_heads = dims->num_q_heads;
@@ -241,7 +250,7 @@ ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* 
   s1.context_lens = context_lens;
   s1.bounds_out = bounds_out;
   s1.status = device_status;
-  return ppa::launch_stage1(s1, false, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return ppa::launch_tile_bounds(s1, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PPA_OK
              : PPA_ERR_CUDA;
 }

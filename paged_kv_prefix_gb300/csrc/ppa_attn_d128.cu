@@ -1,11 +1,12 @@
-// Attention kernel instances for head_dim 128 (bf16 and fp8 e4m3 KV caches).
-#include "ppa_attn.cuh"
+// Attention kernel instances for head_dim 128 (bf16 and fp8 e4m3 KV caches): the
+// warp-specialised two-query-tile kernel.
+#include "ppa_attn_ws.cuh"
 
 namespace ppa {
 
 cudaError_t launch_attn_d128(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream) {
-  return fp8 ? launch_attn<128, true>(p, max_items, stream)
-             : launch_attn<128, false>(p, max_items, stream);
+  return fp8 ? launch_attn_ws<128, true>(p, max_items, stream)
+             : launch_attn_ws<128, false>(p, max_items, stream);
 }
 
 }  // namespace ppa

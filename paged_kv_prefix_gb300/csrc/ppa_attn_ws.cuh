@@ -1,0 +1,728 @@
+// Stage 2: a warp-specialised, pipelined attention kernel for sm_103a.
+//
+// One persistent CTA per SM, 16 warps:
+//   warps 0-3   softmax for query tile A (one thread per row)     \ 192 registers each
+//   warps 4-7   softmax for query tile B                          /
+//   warps 8-11  producers: the paged K/V gather (cp.async) and Q   \ 64 registers each
+//   warp  12    MMA issue (lane 0)                                  |
+//   warps 13-15 idle                                               /
+// A unit of work is two consecutive 128-row query tiles (tq tokens x G heads each, token
+// major) of one sequence and one KV head; both tiles consume one stream of K/V tiles, so each
+// tile is gathered once for 256 query rows. Per key tile kt the MMA warp issues, for each
+// query tile i whose live interval contains kt:
+//     O_i += P_i V(kt)        (P_i read from TMEM: the softmax wrote it over S_i)
+//     S_i  = Q_i K(kt+1)^T    (next tile, into TMEM)
+// so the softmax of one tile overlaps the MMAs of the other ("ping-pong"). S, P and O live in
+// TMEM (512 columns: O_A, O_B, S_A, S_B). The softmax keeps a stale row maximum and rescales O
+// only when the maximum grows by more than 2^8, so P stays <= 256 and rescales are rare.
+//
+// Synchronisation is by mbarriers only: producers -> MMA (q_full, k_full, v_full), MMA ->
+// producers (q_empty, kv_empty via tcgen05.commit), MMA -> softmax (s_full, o_done), softmax
+// -> MMA (p_full, o_empty). Work items come from the plan's list through a two-slot ring
+// filled by one producer thread (atomic work stealing). Every wait is bounded; after a
+// timeout the CTA raises a shared abort flag, every role leaves its loop, the MMAs in flight
+// are retired and TMEM is freed.
+//
+// Sources: the live-tile intervals and the mask are those of "[Kernel][Gemma4] Prune Triton
+// sliding-window tiles for multimodal prefixes" (实现拆解 2, 关键源码片段) and "[Kernel] Skip
+// fully masked key blocks in windowed Triton prefill" (功能与动机); the per-token paged gather
+// follows the PR #54194 report (功能与动机); the row packing BLOCK_M = BLOCK_Q x
+// num_queries_per_kv is the unified-attention layout of PR #53147 (关键源码片段).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ppa_internal.cuh"
+#include "ppa_kernels.h"
+#include "ppa_ptx.cuh"
+
+namespace ppa {
+
+template <int D>
+struct WsCfg {
+  static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+  static constexpr int M = kRowsPerTile;  // rows per query tile
+  // D <= 128: two query tiles share each 128-key tile (S_A, S_B, O_A, O_B fill TMEM).
+  // D = 256: one query tile (O takes 256 columns) with a double-buffered S of 64-key tiles.
+  static constexpr int NQ = D <= 128 ? 2 : 1;  // query tiles per unit
+  static constexpr int TN = D <= 128 ? 128 : 64;  // keys per key tile
+  static constexpr int NSB = NQ == 2 ? 1 : 2;  // S buffers per query tile
+  static constexpr int NS = D == 64 ? 4 : 2;  // K/V pipeline stages
+  static constexpr int CPR = D / 8;       // 16-byte chunks per bf16 row
+  static constexpr int Q_BYTES = M * D * 2;
+  static constexpr int KV_BYTES = TN * D * 2;
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;  // stage s: K at +2s*KV, V at +(2s+1)*KV
+  static constexpr int BAR_OFF = KV_OFF + NS * 2 * KV_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr int TM_O = 0;       // O_i at column TM_O + i*D
+  static constexpr int TM_S = NQ * D;  // S buffer (i, b) at TM_S + (i*NSB + b)*TN; P over its first TN/2
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 512;
+  static_assert(TM_S + NQ * NSB * TN <= TMEM_COLS, "TMEM");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(NQ == tiles_per_unit(D), "plan and kernel agree on query tiles per unit");
+  static_assert(TN == keys_per_tile(D), "plan and kernel agree on the key tile");
+};
+
+// Barrier and slot offsets inside the barrier block.
+namespace wsbar {
+constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL = 48,
+              V_FULL = 80, KV_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
+              O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224;
+constexpr int kRingConsumers = 13;  // warps 0..12 each release a ring slot once
+}  // namespace wsbar
+
+struct WsShared {
+  uint32_t bars;  // shared address of the barrier block
+  volatile int* abort;
+  volatile int* ring;
+  int32_t* status;
+  __device__ uint32_t bar(int off) const { return bars + off; }
+  // Bounded wait; false if the CTA is aborting (this or another role timed out).
+  __device__ bool wait(int off, uint32_t parity) const {
+    const uint32_t b = bars + off;
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait(b, parity)) return true;
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > PPA_WAIT_NS) {
+        *abort = 1;
+        report(status, PPA_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+};
+
+// Consumer side of the item ring (whole warp): the k-th item of this CTA, or -1 at the end.
+__device__ __forceinline__ int ring_get(const WsShared& sh, int k) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
+  return item;
+}
+
+// Single-thread consumer (the MMA issuer): same protocol without the warp.
+__device__ __forceinline__ int ring_get1(const WsShared& sh, int k) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
+  mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
+  return item;
+}
+
+// Producer side (one thread): fetch the next item and publish it in slot k & 1.
+__device__ __forceinline__ void ring_put(const WsShared& sh, const AttnParams& p, int k,
+                                         int n_items) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_EMPTY + 8 * slot, ((k >> 1) & 1) ^ 1)) {
+    item = atomicAdd(&p.ws->next_item, 1);
+    if (item >= n_items) item = -1;
+  }
+  sh.ring[slot] = item;
+  mbar_arrive(sh.bar(wsbar::ITEM_FULL + 8 * slot));
+}
+
+struct UnitInfo {
+  int b, g, t0, nt, c, n, s, q_start, lo, hi;
+  int lo_i[2], hi_i[2];
+};
+
+__device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
+  UnitInfo u;
+  const int packed = p.items[item];
+  const Unit un = p.units[packed / p.num_kv_heads];
+  u.g = packed % p.num_kv_heads;
+  u.b = un.seq;
+  u.t0 = un.t0;
+  u.nt = un.nt;
+  u.c = p.context_lens[u.b];
+  u.q_start = p.cu_query_lens[u.b];
+  u.n = p.cu_query_lens[u.b + 1] - u.q_start;
+  u.s = u.c + u.n;
+  u.lo_i[0] = un.lo0;
+  u.hi_i[0] = un.hi0;
+  u.lo_i[1] = un.nt > 1 ? un.lo1 : 0;
+  u.hi_i[1] = un.nt > 1 ? un.hi1 : 0;
+  u.lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
+  u.hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
+  return u;
+}
+
+__device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
+  return static_cast<uint32_t>((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------------------
+// Producer role (warps 8-11). All four warps load the Q tiles of an item (warp pw owns rows
+// 32*pw .. 32*pw+31). Key tiles alternate between two warp pairs (tile kv_iter goes to pair
+// kv_iter % 2, so with an even number of stages each stage always has the same pair); within
+// a pair, warp h owns rows TN/2*h .. TN/2*h+TN/2-1. A pair issues K then V of its tile, waits for its
+// own copies, fences them for the tensor cores and arrives on k_full / v_full, so the two
+// pairs keep two tiles in flight and no signal waits on a later stage.
+// ---------------------------------------------------------------------------------------
+template <int D, bool FP8>
+__device__ __forceinline__ void gather_rows(const AttnParams& p, const UnitInfo& u, int kt,
+                                            int row0, const char* mine, uint32_t sX) {
+  using C = WsCfg<D>;
+  const int lane = threadIdx.x & 31;
+  if constexpr (!FP8) {
+    constexpr int RPI = 32 / C::CPR;  // rows per warp instruction
+#pragma unroll
+    for (int it = 0; it < 32 / RPI; ++it) {
+      const int lr = it * RPI + lane / C::CPR;
+      const int ch = lane % C::CPR;
+      const char* rp = reinterpret_cast<const char*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr));
+      cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
+                  rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
+    }
+  } else {
+    constexpr int UPR = D / 16;    // 16-element units per row
+    constexpr int RPU = 32 / UPR;  // rows per warp instruction
+    const int jc = u.c - (kt * C::TN + row0);  // local rows below jc are fp8 cache rows
+#pragma unroll
+    for (int it = 0; it < 32 / RPU; ++it) {
+      const int lr = it * RPU + lane / UPR;
+      const int un = lane % UPR;
+      const char* rp = reinterpret_cast<const char*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr));
+      const uint32_t o0 = swz128(row0 + lr, 2 * un, C::TN);
+      const uint32_t o1 = swz128(row0 + lr, 2 * un + 1, C::TN);
+      if (lr < jc) {  // widen fp8 to bf16 here
+        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (rp) {
+          const uint4 codes = ld_global_nc_v4(rp + un * 16);
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            v[2 * q4] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] & 0xFFFFu));
+            v[2 * q4 + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] >> 16));
+          }
+        }
+        st_shared_v4(sX + o0, v[0], v[1], v[2], v[3]);
+        st_shared_v4(sX + o1, v[4], v[5], v[6], v[7]);
+      } else {
+        const char* fb = static_cast<const char*>(p.k_new);
+        cp_async_16(sX + o0, rp ? rp + un * 32 : fb, rp ? 16u : 0u);
+        cp_async_16(sX + o1, rp ? rp + un * 32 + 16 : fb, rp ? 16u : 0u);
+      }
+    }
+  }
+}
+
+template <int D, bool FP8>
+__device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t base, int n_items) {
+  using C = WsCfg<D>;
+  static_assert(C::NS % 2 == 0, "stages alternate between two warp pairs");
+  const int lane = threadIdx.x & 31;
+  const int pw = (threadIdx.x >> 5) - 8;  // 0..3
+  const int pair = pw >> 1, half = pw & 1;
+  const bool leader = pw == 0 && lane == 0;
+  uint32_t kv_iter = 0, q_phase = 0;
+  constexpr size_t kCacheElt = FP8 ? 1 : 2;
+  constexpr int RPI = 32 / C::CPR;  // bf16 rows per warp instruction
+  for (int k = 0;; ++k) {
+    if (leader) ring_put(sh, p, k, n_items);
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
+
+    // ---- Q tiles (zero rows for padding), all four warps ----
+    if (!sh.wait(wsbar::Q_EMPTY, q_phase ^ 1)) break;
+    q_phase ^= 1;
+    for (int i = 0; i < u.nt; ++i) {
+      const uint32_t sQ = base + C::Q_OFF + i * C::Q_BYTES;
+      const int t = u.t0 + i;
+#pragma unroll
+      for (int it = 0; it < 32 / RPI; ++it) {
+        const int row = 32 * pw + it * RPI + lane / C::CPR;
+        const int ch = lane % C::CPR;
+        const int rt = row / p.group, rh = row % p.group, rj = t * p.tq + rt;
+        const bool v = rt < p.tq && rj < u.n;
+        const char* src =
+            static_cast<const char*>(p.q) +
+            (v ? (((size_t)(u.q_start + rj) * p.num_q_heads + u.g * p.group + rh) * D) * 2 + ch * 16
+               : 0);
+        cp_async_16(sQ + swz128(row, ch, C::M), src, v ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    mbar_arrive(sh.bar(wsbar::Q_FULL));
+
+    // ---- K/V tiles of the union interval, alternating between the pairs ----
+    bool ok = true;
+    for (int kt = u.lo; kt < u.hi; ++kt, ++kv_iter) {
+      if ((kv_iter & 1) != (uint32_t)pair) continue;
+      const int s = kv_iter % C::NS;
+      const uint32_t ph = (kv_iter / C::NS) & 1;
+      if (!sh.wait(wsbar::KV_EMPTY + 8 * s, ph ^ 1)) { ok = false; break; }
+      const uint32_t sK = base + C::KV_OFF + (2 * s) * C::KV_BYTES;
+      const uint32_t sV = sK + C::KV_BYTES;
+#pragma unroll
+      for (int sub = 0; sub < C::TN / 64; ++sub) {  // this warp's 32-row blocks
+        const int row0 = (C::TN / 2) * half + 32 * sub;
+        const int pos = kt * C::TN + row0 + lane;
+        const char* kp = nullptr;
+        const char* vp = nullptr;
+        if (pos < u.c) {
+          const int lp = pos / p.page_size;
+          const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
+          if (page >= 0 && page < p.num_pages) {
+            const size_t off =
+                (((size_t)page * p.page_size + (pos - lp * p.page_size)) * p.num_kv_heads + u.g) * D;
+            kp = static_cast<const char*>(p.k_cache) + off * kCacheElt;
+            vp = static_cast<const char*>(p.v_cache) + off * kCacheElt;
+          } else {
+            report(p.status, PPA_ERR_BAD_PAGE);
+          }
+        } else if (pos < u.s) {
+          const size_t off = ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D;
+          kp = static_cast<const char*>(p.k_new) + off * 2;
+          vp = static_cast<const char*>(p.v_new) + off * 2;
+        }
+        gather_rows<D, FP8>(p, u, kt, row0, kp, sK);
+        gather_rows<D, FP8>(p, u, kt, row0, vp, sV);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(wsbar::K_FULL + 8 * s));
+      mbar_arrive(sh.bar(wsbar::V_FULL + 8 * s));
+    }
+    if (!ok) break;
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------------------
+// MMA role (warp 12; lane 0 issues).
+// ---------------------------------------------------------------------------------------
+template <int D>
+__device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, uint32_t tmem) {
+  using C = WsCfg<D>;
+  if ((threadIdx.x & 31) != 0) return;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::TN, false, false);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+  uint32_t kv_iter = 0, q_phase = 0;
+  uint32_t pf_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int item = ring_get1(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
+    if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
+    q_phase ^= 1;
+    tc_fence_after();
+    auto issue_s = [&](int i, int stage) {
+      const uint32_t sQ = base + C::Q_OFF + i * C::Q_BYTES;
+      const uint32_t sK = base + C::KV_OFF + (2 * stage) * C::KV_BYTES;
+      const uint32_t tS = tmem + C::TM_S + i * C::TN;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t db = kk >> 2, ks = kk & 3;
+        mma_bf16_ss(tS, sdesc_sw128(sQ + db * (C::M * 128) + ks * 32, 16, 1024),
+                    sdesc_sw128(sK + db * (C::TN * 128) + ks * 32, 16, 1024), kIdescS,
+                    kk > 0 ? 1u : 0u);
+      }
+      tc_commit(sh.bar(wsbar::S_FULL + 8 * i));
+    };
+    for (int kt = u.lo; kt < u.hi && ok; ++kt) {
+      const int s = kv_iter % C::NS;
+      const uint32_t ph = (kv_iter / C::NS) & 1;
+      // first key tile of a query tile: its S
+      for (int i = 0; i < u.nt && ok; ++i) {
+        if (kt != u.lo_i[i]) continue;
+        if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(i, s);
+      }
+      for (int i = 0; i < u.nt && ok; ++i) {
+        if (kt < u.lo_i[i] || kt >= u.hi_i[i]) continue;
+        if (kt == u.lo_i[i]) {  // O_i must have been read out by the previous epilogue
+          if (!sh.wait(wsbar::O_EMPTY + 8 * i, oe_phase[i] ^ 1)) { ok = false; break; }
+          oe_phase[i] ^= 1;
+        }
+        if (!sh.wait(wsbar::P_FULL + 8 * i, pf_phase[i])) { ok = false; break; }
+        pf_phase[i] ^= 1;
+        if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sV = base + C::KV_OFF + (2 * s + 1) * C::KV_BYTES;
+        const uint32_t tP = tmem + C::TM_S + i * C::TN;
+        const uint32_t tO = tmem + C::TM_O + i * D;
+#pragma unroll
+        for (int kk = 0; kk < C::TN / 16; ++kk) {
+          mma_bf16_ts(tO, tP + kk * 8, sdesc_sw128(sV + kk * 16 * 128, C::TN * 128, 1024),
+                      kIdescO, (kt > u.lo_i[i] || kk > 0) ? 1u : 0u);
+        }
+        if (kt + 1 < u.hi_i[i]) {
+          const int s2 = (kv_iter + 1) % C::NS;
+          const uint32_t ph2 = ((kv_iter + 1) / C::NS) & 1;
+          if (!sh.wait(wsbar::K_FULL + 8 * s2, ph2)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(i, s2);
+        } else {
+          tc_commit(sh.bar(wsbar::O_DONE + 8 * i));
+        }
+      }
+      tc_commit(sh.bar(wsbar::KV_EMPTY + 8 * s));
+      ++kv_iter;
+    }
+    tc_commit(sh.bar(wsbar::Q_EMPTY));
+  }
+}
+
+// MMA role for one query tile per unit (D = 256): S is double-buffered, so S(kt+1) is issued
+// before PV(kt) and the softmax of tile kt overlaps both. One commit to O_DONE per PV lets the
+// softmax know when O is idle (for a rescale) and when it is final (epilogue).
+template <int D>
+__device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t base,
+                              uint32_t tmem) {
+  using C = WsCfg<D>;
+  if ((threadIdx.x & 31) != 0) return;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::TN, false, false);
+  constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+  uint32_t kv_iter = 0, q_phase = 0, pf_phase = 0, oe_phase = 0, sc = 0;
+  const uint32_t sQ = base + C::Q_OFF;
+  auto issue_s = [&](int stage, uint32_t buf) {
+    const uint32_t sK = base + C::KV_OFF + (2 * stage) * C::KV_BYTES;
+    const uint32_t tS = tmem + C::TM_S + buf * C::TN;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t db = kk >> 2, ks = kk & 3;
+      mma_bf16_ss(tS, sdesc_sw128(sQ + db * (C::M * 128) + ks * 32, 16, 1024),
+                  sdesc_sw128(sK + db * (C::TN * 128) + ks * 32, 16, 1024), kIdescS,
+                  kk > 0 ? 1u : 0u);
+    }
+    tc_commit(sh.bar(wsbar::S_FULL + 8 * buf));
+  };
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int item = ring_get1(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
+    if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
+    q_phase ^= 1;
+    tc_fence_after();
+    for (int kt = u.lo; kt < u.hi; ++kt) {
+      const int s = kv_iter % C::NS;
+      const uint32_t ph = (kv_iter / C::NS) & 1;
+      if (kt == u.lo) {
+        if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(s, sc & 1);
+      }
+      if (kt + 1 < u.hi) {
+        const int s2 = (kv_iter + 1) % C::NS;
+        if (!sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / C::NS) & 1)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(s2, (sc + 1) & 1);
+      }
+      if (kt == u.lo) {  // O must have been read out by the previous epilogue
+        if (!sh.wait(wsbar::O_EMPTY, oe_phase ^ 1)) { ok = false; break; }
+        oe_phase ^= 1;
+      }
+      if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }
+      pf_phase ^= 1;
+      if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sV = base + C::KV_OFF + (2 * s + 1) * C::KV_BYTES;
+      const uint32_t tP = tmem + C::TM_S + (sc & 1) * C::TN;
+#pragma unroll
+      for (int kk = 0; kk < C::TN / 16; ++kk) {
+        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8,
+                    sdesc_sw128(sV + kk * 16 * 128, C::TN * 128, 1024), kIdescO,
+                    (kt > u.lo || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(sh.bar(wsbar::O_DONE));
+      tc_commit(sh.bar(wsbar::KV_EMPTY + 8 * s));
+      ++kv_iter;
+      ++sc;
+    }
+    tc_commit(sh.bar(wsbar::Q_EMPTY));
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Softmax role (warps 0-7): warpgroup i owns query tile i; thread r owns row r.
+// ---------------------------------------------------------------------------------------
+template <int D, bool FP8>
+__device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tmem) {
+  using C = WsCfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int i = warp >> 2;
+  const int r = threadIdx.x & 127;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tO = tmem + C::TM_O + i * D + lane_off;
+  const float neg_inf = -__int_as_float(0x7f800000);
+  const float scale = p.scale_log2;
+  // NQ == 2: one S buffer per tile, S_FULL[i] and O_DONE[i] flip once per use.
+  // NQ == 1: S buffers alternate (tile count sc), O_DONE completes once per PV.
+  uint32_t sf_phase = 0, od_phase = 0, sc = 0;
+  for (int k = 0;; ++k) {
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
+    if (i >= u.nt) continue;
+    const int lo = u.lo_i[i], hi = u.hi_i[i];
+    const int tok = r / p.group, hh = r % p.group;
+    const int j = (u.t0 + i) * p.tq + tok;
+    const bool row_valid = tok < p.tq && j < u.n;
+    int kmin = 0, kmax = u.s - 1;  // padding rows attend everywhere (Q is zero: finite)
+    if (row_valid) {
+      const int32_t* ranges =
+          p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)u.b * p.mask.max_mm_ranges * 2 : nullptr;
+      row_interval(u.c + j, u.s, p.mask, ranges, kmin, kmax);
+    }
+    float ks_ctx = 1.f, vs_ctx = 1.f;
+    if constexpr (FP8) {
+      ks_ctx = *p.k_scale;
+      vs_ctx = *p.v_scale;
+    }
+    float m_ref = neg_inf, l_run = 0.f;
+    bool ok = true;
+    for (int kt = lo; kt < hi; ++kt) {
+      const uint32_t buf = C::NQ == 2 ? 0u : (sc & 1);
+      const uint32_t tS = tmem + C::TM_S + (i * C::NSB + buf) * C::TN + lane_off;
+      if constexpr (C::NQ == 2) {
+        if (!sh.wait(wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
+        sf_phase ^= 1;
+      } else {
+        if (!sh.wait(wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
+      }
+      ++sc;
+      tc_fence_after();
+      float sv[C::TN];
+#pragma unroll
+      for (int cc = 0; cc < C::TN / 64; ++cc) {
+        uint32_t r64[64];
+        tmem_ld_64(tS + cc * 64, r64);
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
+      }
+      const int k0 = kt * C::TN;
+      if constexpr (FP8) {  // cache columns carry the K dequantisation scale
+        const int jc = min(max(u.c - k0, 0), C::TN);
+#pragma unroll
+        for (int e = 0; e < C::TN; ++e) sv[e] = e < jc ? sv[e] * ks_ctx : sv[e];
+      }
+      const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
+      if (!(a0 <= 0 && a1 >= C::TN - 1)) {
+#pragma unroll
+        for (int e = 0; e < C::TN; ++e) sv[e] = (e < a0 || e > a1) ? neg_inf : sv[e];
+      }
+      float mx[8];
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) mx[q8] = sv[q8];
+#pragma unroll
+      for (int e = 8; e < C::TN; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+      const float tile_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_tile = tile_max * scale;  // in exp2 units
+      // Keep the stale reference unless the maximum grew by more than 2^8.
+      bool rescale = false;
+      float alpha = 1.f;
+      if (m_tile > m_ref + 8.f) {
+        alpha = ex2_approx(m_ref - m_tile);  // 0 when m_ref = -inf
+        rescale = kt > lo;
+        m_ref = m_tile;
+      }
+      const float m_use = m_ref == neg_inf ? 0.f : m_ref;
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[C::TN / 2];
+#pragma unroll
+      for (int e = 0; e < C::TN; e += 2) {
+        float p0 = ex2_approx(fmaf(sv[e], scale, -m_use));
+        float p1 = ex2_approx(fmaf(sv[e + 1], scale, -m_use));
+        sum[(e >> 1) & 7] += p0 + p1;
+        if constexpr (FP8) {
+          const int jc = min(max(u.c - k0, 0), C::TN);
+          p0 = e < jc ? p0 * vs_ctx : p0;
+          p1 = e + 1 < jc ? p1 * vs_ctx : p1;
+        }
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha +
+              (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+      // P over the first TN/2 columns of this S buffer
+#pragma unroll
+      for (int cc = 0; cc < C::TN / 64; ++cc) {
+        uint32_t w32[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w32[e] = pk[cc * 32 + e];
+        tmem_st_32(tS + cc * 32, w32);
+      }
+      // NQ == 2: O_i is idle here, PV_i(kt-1) completed before S_i(kt) (one issuing thread,
+      // in order). NQ == 1: S(kt) was issued before PV(kt-1), so wait for that PV first.
+      if constexpr (C::NQ == 1) {
+        if (kt > lo) {
+          if (!sh.wait(wsbar::O_DONE, od_phase)) { ok = false; break; }
+          od_phase ^= 1;
+          tc_fence_after();
+        }
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o32[32];
+          tmem_ld_32(tO + cc * 32, o32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o32[e] = __float_as_uint(__uint_as_float(o32[e]) * alpha);
+          tmem_st_32(tO + cc * 32, o32);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sh.bar(wsbar::P_FULL + 8 * i));
+    }
+    if (!ok) break;
+    // ---- epilogue: the last PV of this tile ----
+    if (!sh.wait(wsbar::O_DONE + 8 * i, od_phase)) break;
+    od_phase ^= 1;
+    tc_fence_after();
+    const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+    __nv_bfloat16* orow =
+        static_cast<__nv_bfloat16*>(p.out) +
+        ((size_t)(u.q_start + (row_valid ? j : 0)) * p.num_q_heads + u.g * p.group + hh) * D;
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t o32[32];
+      tmem_ld_32(tO + cc * 32, o32);
+      if (row_valid) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(o32[2 * e]) * inv_l,
+                             __uint_as_float(o32[2 * e + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(sh.bar(wsbar::O_EMPTY + 8 * i));
+  }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(512, 1) attn_ws_kernel(const AttnParams p) {
+  using C = WsCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  uint8_t* barp = smem + C::BAR_OFF;
+  WsShared sh;
+  sh.bars = base + C::BAR_OFF;
+  sh.abort = reinterpret_cast<volatile int*>(barp + wsbar::ABORT);
+  sh.ring = reinterpret_cast<volatile int*>(barp + wsbar::RING);
+  sh.status = p.status;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  if (tid == 0) {
+    using namespace wsbar;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sh.bar(ITEM_FULL + 8 * s), 1);
+      mbar_init(sh.bar(ITEM_EMPTY + 8 * s), kRingConsumers);
+      mbar_init(sh.bar(S_FULL + 8 * s), 1);
+      mbar_init(sh.bar(P_FULL + 8 * s), 128);
+      mbar_init(sh.bar(O_DONE + 8 * s), 1);
+      mbar_init(sh.bar(O_EMPTY + 8 * s), 128);
+    }
+    mbar_init(sh.bar(Q_FULL), 128);
+    mbar_init(sh.bar(Q_EMPTY), 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(sh.bar(K_FULL + 8 * s), 64);  // the 64 threads of the pair that owns stage s
+      mbar_init(sh.bar(V_FULL + 8 * s), 64);
+      mbar_init(sh.bar(KV_EMPTY + 8 * s), 1);
+    }
+    mbar_init(sh.bar(FIN), 1);
+    *sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(sh.bar(wsbar::TMEM_SLOT), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(barp + wsbar::TMEM_SLOT);
+  const int n_items = p.ws->n_items;
+
+  if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
+    ws_softmax<D, FP8>(p, sh, tmem);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    if (warp < 12) {
+      ws_producer<D, FP8>(p, sh, base, n_items);
+    } else if (warp == 12) {
+      if constexpr (C::NQ == 2) {
+        ws_mma<D>(p, sh, base, tmem);
+      } else {
+        ws_mma_single<D>(p, sh, base, tmem);
+      }
+      if ((tid & 31) == 0) {  // retire every MMA this CTA issued before TMEM is freed
+        tc_commit(sh.bar(wsbar::FIN));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(sh.bar(wsbar::FIN), 0)) {
+          if (globaltimer_ns() - t0 > PPA_WAIT_NS) {
+            report(p.status, PPA_ERR_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  // The last CTA to finish re-arms the work counter for the next launch on this plan.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&p.ws->done_ctas, 1) == (int)gridDim.x - 1) {
+      p.ws->next_item = 0;
+      p.ws->done_ctas = 0;
+      __threadfence();
+    }
+  }
+}
+
+template <int D, bool FP8>
+cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stream) {
+  using C = WsCfg<D>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int configured[64] = {0};
+  static int sm_count[64] = {0};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(attn_ws_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  const int grid = max(1, min(sm_count[dev], max_items));
+  attn_ws_kernel<D, FP8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ppa

@@ -21,18 +21,20 @@ struct MaskParams {
   const int32_t* mm_ranges;  // [B][R][2] or nullptr
 };
 
-// Workspace header; followed by the query-tile table and the work list.
+// Workspace header; followed by per-sequence arrays, the unit table and the work list.
 struct WsHeader {
   int32_t next_item;   // work-stealing counter of the persistent kernel
-  int32_t n_items;     // number of (query tile, kv head) items, 0 on a device-side error
-  int32_t n_qtiles;
+  int32_t n_items;     // number of (unit, kv head) items, 0 on a device-side error
+  int32_t n_units;
   int32_t done_ctas;   // CTAs of the running attention launch that have finished
   int32_t pad[12];
 };
 
-// One query tile: sequence, tile index within the sequence, live key tiles [lo, hi).
-struct QTile {
-  int32_t seq, t, lo, hi;
+// One unit of work: nt (1 or 2) consecutive query tiles t0, t0+1 of sequence `seq` that
+// share one K/V stream, with each tile's live key tiles [lo_i, hi_i). `cost` is the number of
+// key tiles in the union.
+struct Unit {
+  int32_t seq, t0, nt, lo0, hi0, lo1, hi1, cost;
 };
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
@@ -111,7 +113,7 @@ __device__ __forceinline__ void tile_interval(int q_lo, int q_hi, int s, const M
 }
 
 // Tile shape for a head group of G query heads: tq tokens x G heads <= 128 rows.
-__host__ __device__ inline int tokens_per_qtile(int group) { return kRowsPerTile / group; }
-__host__ __device__ inline int keys_per_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+__host__ __device__ constexpr int tokens_per_qtile(int group) { return kRowsPerTile / group; }
+__host__ __device__ constexpr int keys_per_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 
 }  // namespace ppa

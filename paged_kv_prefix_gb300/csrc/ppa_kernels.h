@@ -12,14 +12,21 @@ namespace ppa {
 
 struct Stage1Params {
   int num_seqs, total_q, tq, tn, num_kv_heads, page_size, max_pages_per_seq, no_prune;
-  int max_qtiles;
+  int max_qtiles;       // bound on sum_b ceil(n_b / tq); also bounds the number of units
+  int nq;               // query tiles per unit (plan mode)
   MaskParams mask;
   const int32_t* cu_query_lens;
   const int32_t* context_lens;
-  WsHeader* ws;         // work-list mode
-  QTile* qtiles;        // work-list mode: [max_qtiles]
-  int32_t* order;       // work-list mode: [max_qtiles], query tiles heaviest first
-  int32_t* bounds_out;  // bounds-only mode: [max_qtiles][2]
+  // plan mode
+  WsHeader* ws;
+  int32_t* seq_unit_base;  // [B + 1] first unit of each sequence (sequence order)
+  int32_t* seq_cost;       // [B]     key tiles summed over the sequence's units
+  int32_t* seq_order;      // [B]     sequences, heaviest first
+  int32_t* seq_item_base;  // [B + 1] first item of each sequence in heaviest-first order
+  Unit* units;             // [max_qtiles]
+  int32_t* items;          // [max_qtiles * num_kv_heads]: unit * Hkv + kv head
+  // bounds-only mode
+  int32_t* bounds_out;     // [max_qtiles][2]
   int32_t* status;
 };
 
@@ -36,15 +43,20 @@ struct AttnParams {
   const float* v_scale;  // fp8 only
   void* out;
   WsHeader* ws;
-  const QTile* qtiles;
-  const int32_t* order;
+  const Unit* units;
+  const int32_t* items;
   int32_t* status;
   MaskParams mask;
   int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
   float scale_log2;  // softmax scale * log2(e)
 };
 
-cudaError_t launch_stage1(const Stage1Params& p, bool worklist, cudaStream_t stream);
+cudaError_t launch_plan(const Stage1Params& p, cudaStream_t stream);
+cudaError_t launch_tile_bounds(const Stage1Params& p, cudaStream_t stream);
+
+// Query tiles per unit of work for a head dimension: two 128-row tiles share each K/V tile
+// when both fit in TMEM and shared memory (D <= 128), otherwise one.
+__host__ __device__ constexpr int tiles_per_unit(int head_dim) { return head_dim <= 128 ? 2 : 1; }
 cudaError_t launch_debug_mask(const MaskParams& mp, int seq, const int32_t* cu, const int32_t* ctx,
                               uint32_t* bitmap, int max_rows, int words_per_row,
                               cudaStream_t stream);

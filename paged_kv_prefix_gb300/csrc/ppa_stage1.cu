@@ -21,7 +21,6 @@ namespace ppa {
 namespace {
 
 constexpr int kStage1Threads = 1024;
-constexpr int kCostBins = 2048;  // work-list cost histogram; costs >= 2047 share the last bin
 
 // Inclusive scan across the block (1024 threads); returns the exclusive prefix, sets *total.
 __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -52,84 +51,84 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 }  // namespace
 
-// One CTA of 1024 threads. Sequences are taken 1024 at a time: each thread validates one
-// sequence and counts its query tiles, a block scan turns counts into tile offsets, then the
-// chunk's tiles are spread over the threads (a binary search finds a tile's sequence).
-template <bool kWorklist>
-__global__ void __launch_bounds__(kStage1Threads) stage1_kernel(const Stage1Params p) {
+// Validates sequence b and returns its query length (0 if invalid, with *bad set).
+__device__ __forceinline__ int seq_query_len(const Stage1Params& p, int b, int* c_out, bool* bad) {
+  const int q0 = p.cu_query_lens[b], q1 = p.cu_query_lens[b + 1];
+  const int c = p.context_lens[b];
+  const int n = q1 - q0;
+  bool ok = (n >= 0) && (c >= 0) && (q0 >= 0) && (c <= INT_MAX - n);
+  if (b == 0 && q0 != 0) ok = false;
+  if (b == p.num_seqs - 1 && q1 != p.total_q) ok = false;
+  if (ok && c > 0 && (c - 1) / p.page_size >= p.max_pages_per_seq) ok = false;
+  *c_out = c;
+  if (!ok) *bad = true;
+  return ok ? n : 0;
+}
+
+// Live key tiles of query tile t of a sequence (context c, n queries).
+__device__ __forceinline__ void qtile_bounds(const Stage1Params& p, int seq, int c, int n, int t,
+                                             int* lo, int* hi) {
+  const int s = c + n;
+  if (p.no_prune) {
+    *lo = 0;
+    *hi = (s + p.tn - 1) / p.tn;
+    return;
+  }
+  const int q_lo = c + t * p.tq;
+  const int q_hi = c + min(n, (t + 1) * p.tq) - 1;
+  const int32_t* ranges =
+      p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)seq * p.mask.max_mm_ranges * 2 : nullptr;
+  int klo, khi;
+  tile_interval(q_lo, q_hi, s, p.mask, ranges, klo, khi);
+  *lo = klo / p.tn;
+  *hi = khi / p.tn + 1;
+}
+
+// Last index r in [0, count) with base[r] <= x (base non-decreasing, base[0] <= x).
+__device__ __forceinline__ int last_le(const int32_t* base, int count, int x) {
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (base[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Bounds only (testing): {lo, hi} of every query tile, in (sequence, tile) order.
+__global__ void __launch_bounds__(kStage1Threads) tile_bounds_kernel(const Stage1Params p) {
   __shared__ int s_base[kStage1Threads];
   __shared__ int s_c[kStage1Threads];
   __shared__ int s_n[kStage1Threads];
   __shared__ int s_warp[32];
-  __shared__ int s_hist[kWorklist ? kCostBins : 1];
   __shared__ int s_err;
-
   const int tid = threadIdx.x;
   if (tid == 0) s_err = 0;
-  if (kWorklist) {
-    for (int i = tid; i < kCostBins; i += kStage1Threads) s_hist[i] = 0;
-  }
   __syncthreads();
-
-  int carry = 0;  // query tiles of the sequences before this chunk
+  int carry = 0;
   for (int b0 = 0; b0 < p.num_seqs; b0 += kStage1Threads) {
     const int b = b0 + tid;
     int nt = 0, c = 0, n = 0;
     if (b < p.num_seqs) {
-      const int q0 = p.cu_query_lens[b], q1 = p.cu_query_lens[b + 1];
-      c = p.context_lens[b];
-      n = q1 - q0;
-      bool ok = (n >= 0) && (c >= 0) && (q0 >= 0) && (c <= INT_MAX - n);
-      if (b == 0 && q0 != 0) ok = false;
-      if (b == p.num_seqs - 1 && q1 != p.total_q) ok = false;
-      if (ok && c > 0 && (c - 1) / p.page_size >= p.max_pages_per_seq) ok = false;
-      if (!ok) {
-        atomicExch(&s_err, 1);
-        n = 0;
-      }
+      bool bad = false;
+      n = seq_query_len(p, b, &c, &bad);
+      if (bad) atomicExch(&s_err, 1);
       nt = (n + p.tq - 1) / p.tq;
     }
     int total;
     const int excl = block_exclusive_scan(nt, s_warp, &total);
-    s_base[tid] = excl;  // offset within this chunk
+    s_base[tid] = excl;
     s_c[tid] = c;
     s_n[tid] = n;
     __syncthreads();
     const int nseq = min(kStage1Threads, p.num_seqs - b0);
     for (int i = tid; i < total; i += kStage1Threads) {
-      // the last sequence of the chunk whose base is <= i
-      int lo = 0, hi = nseq - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_base[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      const int sb = lo;
-      const int t = i - s_base[sb];
-      const int seq = b0 + sb;
-      const int cs = s_c[sb], ns = s_n[sb], s = cs + ns;
-      const int q_lo = cs + t * p.tq;
-      const int q_hi = cs + min(ns, (t + 1) * p.tq) - 1;
-      int lo_t, hi_t;
-      if (p.no_prune) {
-        lo_t = 0;
-        hi_t = (s + p.tn - 1) / p.tn;
-      } else {
-        const int32_t* ranges =
-            p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)seq * p.mask.max_mm_ranges * 2 : nullptr;
-        int klo, khi;
-        tile_interval(q_lo, q_hi, s, p.mask, ranges, klo, khi);
-        lo_t = klo / p.tn;
-        hi_t = khi / p.tn + 1;
-      }
+      const int sb = last_le(s_base, nseq, i);
+      int lo, hi;
+      qtile_bounds(p, b0 + sb, s_c[sb], s_n[sb], i - s_base[sb], &lo, &hi);
       const int gi = carry + i;
       if (gi < p.max_qtiles) {
-        if (kWorklist) {
-          p.qtiles[gi] = QTile{seq, t, lo_t, hi_t};
-          atomicAdd(&s_hist[min(hi_t - lo_t, kCostBins - 1)], 1);
-        } else {
-          p.bounds_out[2 * gi] = lo_t;
-          p.bounds_out[2 * gi + 1] = hi_t;
-        }
+        p.bounds_out[2 * gi] = lo;
+        p.bounds_out[2 * gi + 1] = hi;
       } else {
         atomicExch(&s_err, 1);
       }
@@ -137,39 +136,127 @@ __global__ void __launch_bounds__(kStage1Threads) stage1_kernel(const Stage1Para
     carry += total;
     __syncthreads();
   }
+  if (s_err && tid == 0) report(p.status, PPA_ERR_INVALID);
+}
 
-  if (s_err) {
-    if (tid == 0) report(p.status, PPA_ERR_INVALID);
-    if (kWorklist && tid == 0) {
+// The plan (one CTA of 1024 threads):
+//   1. validate every sequence and count its units (nq query tiles each); scan -> unit bases;
+//   2. every unit's per-tile live key-tile intervals and union cost; per-sequence cost;
+//   3. rank sequences by cost, heaviest first (up to kMaxRankedSeqs; beyond that, in order);
+//   4. lay the work list out sequence by sequence in that rank order, KV head by KV head,
+//      each sequence's units last-to-first. The query tiles of one (sequence, KV head) are
+//      thus taken together by neighbouring CTAs and stream the same K/V through L2, while
+//      the heaviest sequences start first.
+constexpr int kMaxRankedSeqs = 4096;
+
+__global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params p) {
+  __shared__ int s_warp[32];
+  __shared__ int s_err;
+  const int tid = threadIdx.x;
+  const int B = p.num_seqs;
+  if (tid == 0) s_err = 0;
+  __syncthreads();
+
+  // 1. units per sequence
+  int carry = 0;
+  for (int b0 = 0; b0 < B; b0 += kStage1Threads) {
+    const int b = b0 + tid;
+    int nu = 0;
+    if (b < B) {
+      bool bad = false;
+      int c;
+      const int n = seq_query_len(p, b, &c, &bad);
+      if (bad) atomicExch(&s_err, 1);
+      const int nt = (n + p.tq - 1) / p.tq;
+      nu = (nt + p.nq - 1) / p.nq;
+      p.seq_cost[b] = 0;
+    }
+    int total;
+    const int excl = block_exclusive_scan(nu, s_warp, &total);
+    if (b < B) p.seq_unit_base[b] = carry + excl;
+    carry += total;
+  }
+  const int n_units = carry;
+  if (tid == 0) p.seq_unit_base[B] = n_units;
+  __syncthreads();
+  if (s_err || n_units > p.max_qtiles || (long long)n_units * p.num_kv_heads > INT_MAX) {
+    if (tid == 0) {
+      report(p.status, PPA_ERR_INVALID);
       p.ws->n_items = 0;
-      p.ws->n_qtiles = 0;
+      p.ws->n_units = 0;
       p.ws->next_item = 0;
       p.ws->done_ctas = 0;
     }
     return;
   }
-  if (!kWorklist) return;
 
-  // Counting sort of the query tiles by cost (live key tiles), heaviest first, so that the
-  // persistent kernel's work stealing approximates longest-processing-time-first.
-  const int n_qtiles = carry;
-  if (tid == 0) {
-    int run = 0;
-    for (int bin = kCostBins - 1; bin >= 0; --bin) {
-      const int h = s_hist[bin];
-      s_hist[bin] = run;
-      run += h;
+  // 2. units
+  for (int u = tid; u < n_units; u += kStage1Threads) {
+    const int b = last_le(p.seq_unit_base, B, u);
+    const int c = p.context_lens[b];
+    const int n = p.cu_query_lens[b + 1] - p.cu_query_lens[b];
+    const int nt = (n + p.tq - 1) / p.tq;
+    const int t0 = (u - p.seq_unit_base[b]) * p.nq;
+    const int cnt = min(p.nq, nt - t0);
+    Unit un{b, t0, cnt, 0, 0, 0, 0, 0};
+    qtile_bounds(p, b, c, n, t0, &un.lo0, &un.hi0);
+    int lo = un.lo0, hi = un.hi0;
+    if (cnt > 1) {
+      qtile_bounds(p, b, c, n, t0 + 1, &un.lo1, &un.hi1);
+      lo = min(lo, un.lo1);
+      hi = max(hi, un.hi1);
     }
+    un.cost = hi - lo;
+    p.units[u] = un;
+    atomicAdd(&p.seq_cost[b], un.cost);
   }
   __syncthreads();
-  for (int i = tid; i < n_qtiles; i += kStage1Threads) {
-    const QTile qt = p.qtiles[i];
-    const int pos = atomicAdd(&s_hist[min(qt.hi - qt.lo, kCostBins - 1)], 1);
-    p.order[pos] = i;
+
+  // 3. sequences heaviest first (ties by index)
+  for (int b = tid; b < B; b += kStage1Threads) {
+    int rank = b;
+    if (B <= kMaxRankedSeqs) {
+      const int cb = p.seq_cost[b];
+      rank = 0;
+      for (int b2 = 0; b2 < B; ++b2) {
+        const int c2 = p.seq_cost[b2];
+        rank += (c2 > cb) || (c2 == cb && b2 < b);
+      }
+    }
+    p.seq_order[rank] = b;
+  }
+  __syncthreads();
+
+  // 4. item bases in rank order, then the items
+  carry = 0;
+  for (int r0 = 0; r0 < B; r0 += kStage1Threads) {
+    const int r = r0 + tid;
+    int cnt = 0;
+    if (r < B) {
+      const int b = p.seq_order[r];
+      cnt = (p.seq_unit_base[b + 1] - p.seq_unit_base[b]) * p.num_kv_heads;
+    }
+    int total;
+    const int excl = block_exclusive_scan(cnt, s_warp, &total);
+    if (r < B) p.seq_item_base[r] = carry + excl;
+    carry += total;
+  }
+  const int n_items = carry;
+  if (tid == 0) p.seq_item_base[B] = n_items;
+  __syncthreads();
+  for (int i = tid; i < n_items; i += kStage1Threads) {
+    const int r = last_le(p.seq_item_base, B, i);
+    const int b = p.seq_order[r];
+    const int ub = p.seq_unit_base[b];
+    const int nu = p.seq_unit_base[b + 1] - ub;
+    const int li = i - p.seq_item_base[r];
+    const int g = li / nu;
+    const int lu = nu - 1 - (li - g * nu);
+    p.items[i] = (ub + lu) * p.num_kv_heads + g;
   }
   if (tid == 0) {
-    p.ws->n_qtiles = n_qtiles;
-    p.ws->n_items = n_qtiles * p.num_kv_heads;
+    p.ws->n_units = n_units;
+    p.ws->n_items = n_items;
     p.ws->next_item = 0;
     p.ws->done_ctas = 0;
   }
@@ -239,12 +326,13 @@ __global__ void e4m3_decode_kernel(const uint8_t* codes, uint16_t* out, int n) {
 // ---------------------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------------------
-cudaError_t launch_stage1(const Stage1Params& p, bool worklist, cudaStream_t stream) {
-  if (worklist) {
-    stage1_kernel<true><<<1, kStage1Threads, 0, stream>>>(p);
-  } else {
-    stage1_kernel<false><<<1, kStage1Threads, 0, stream>>>(p);
-  }
+cudaError_t launch_plan(const Stage1Params& p, cudaStream_t stream) {
+  plan_kernel<<<1, kStage1Threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_bounds(const Stage1Params& p, cudaStream_t stream) {
+  tile_bounds_kernel<<<1, kStage1Threads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
