@@ -1,11 +1,14 @@
 // The C ABI declared in include/ppa.h: argument validation, workspace sizing and the two
 // launches of ppa_prefill. Nothing here allocates, frees or synchronises, except
 // ppa_read_status, whose job is to synchronise.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/ppa.h"
 #include "ppa_internal.cuh"
@@ -73,6 +76,36 @@ WsLayout ws_layout(const ppa_dims* d) {
   w.items = align_up(w.units + (size_t)mq * sizeof(ppa::Unit), 256);
   w.total = align_up(w.items + (size_t)mq * d->num_kv_heads * 4, 256);
   return w;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A 3-D bf16 tensor [rows][heads][D] (row-major) seen as dims {D, heads, rows}, with a box of
+// {64, box_heads, box_rows} and the 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* ptr, int head_dim, int heads, long long rows,
+                 int box_heads, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -185,6 +218,17 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.page_size = dims->page_size;
   a.num_pages = dims->num_pages;
   a.max_pages_per_seq = dims->max_pages_per_seq;
+  const int D = dims->head_dim;
+  bool maps_ok =
+      encode_rows(&a.tm.q, q, D, dims->num_q_heads, dims->total_q, G, tq) &&
+      encode_rows(&a.tm.k_new, k_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
+      encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16);
+  if (maps_ok && !fp8) {
+    const long long cache_rows = (long long)dims->num_pages * dims->page_size;
+    maps_ok = encode_rows(&a.tm.k_cache, k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
+              encode_rows(&a.tm.v_cache, v_cache, D, dims->num_kv_heads, cache_rows, 1, 16);
+  }
+  if (!maps_ok) return PPA_ERR_CUDA;
   const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);
   a.scale_log2 = sm * 1.4426950408889634f;
   const int max_items = (int)(mq * dims->num_kv_heads);

@@ -3,7 +3,7 @@
 // One persistent CTA per SM, 16 warps:
 //   warps 0-3   softmax for query tile A (one thread per row)     \ 192 registers each
 //   warps 4-7   softmax for query tile B                          /
-//   warps 8-11  producers: the paged K/V gather (cp.async) and Q   \ 64 registers each
+//   warps 8-11  producers: TMA / cp.async paged K/V gather and Q   \ 64 registers each
 //   warp  12    MMA issue (lane 0)                                  |
 //   warps 13-15 idle                                               /
 // A unit of work is two consecutive 128-row query tiles (tq tokens x G heads each, token
@@ -163,42 +163,51 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Producer role (warps 8-11). All four warps load the Q tiles of an item (warp pw owns rows
-// 32*pw .. 32*pw+31). Key tiles alternate between two warp pairs (tile kv_iter goes to pair
-// kv_iter % 2, so with an even number of stages each stage always has the same pair); within
-// a pair, warp h owns rows TN/2*h .. TN/2*h+TN/2-1. A pair issues K then V of its tile, waits for its
-// own copies, fences them for the tensor cores and arrives on k_full / v_full, so the two
-// pairs keep two tiles in flight and no signal waits on a later stage.
+// Producer role (warps 8-11).
+//
+// Q: producer warp 0 loads each query tile with one TMA box per 64-column block; the box
+// {64 columns, G heads, tq tokens} lands as token-major rows, exactly the MMA's A operand.
+// K/V: every producer warp owns a quarter of each key tile (TN/4 rows = one or two chunks of
+// 16 keys). A chunk whose 16 keys are cached context in one page, or are all new tokens, is one
+// TMA box per 64-column block from the cache or the k_new/v_new tensor (rows past the
+// sequence read the next sequence's tokens or the zero fill beyond the tensor: finite values
+// that the mask removes). Any other chunk (it straddles the context end or a page boundary;
+// the page id is out of range; the cache is fp8 and must be widened) is gathered row by row
+// with cp.async, as the PR #54194 report describes for per-token offsets. Each warp then
+// arrives once on k_full / v_full with the byte count of its boxes.
 // ---------------------------------------------------------------------------------------
+
+// Row-wise gather of rows row0 .. row0+nrows-1 whose bit is set in `rowmask`; `mine` is the
+// source row of lane `lane` (lanes >= nrows unused), nullptr for zero fill.
 template <int D, bool FP8>
-__device__ __forceinline__ void gather_rows(const AttnParams& p, const UnitInfo& u, int kt,
-                                            int row0, const char* mine, uint32_t sX) {
+__device__ __forceinline__ void gather_rows(const AttnParams& p, int row0, int nrows,
+                                            uint32_t rowmask, int cache_rows, const char* mine,
+                                            uint32_t sX) {
   using C = WsCfg<D>;
   const int lane = threadIdx.x & 31;
   if constexpr (!FP8) {
     constexpr int RPI = 32 / C::CPR;  // rows per warp instruction
-#pragma unroll
-    for (int it = 0; it < 32 / RPI; ++it) {
+    for (int it = 0; it * RPI < nrows; ++it) {
       const int lr = it * RPI + lane / C::CPR;
       const int ch = lane % C::CPR;
       const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr));
-      cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
-                  rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
+      if (lr < nrows && ((rowmask >> lr) & 1u))
+        cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
+                    rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
     }
   } else {
     constexpr int UPR = D / 16;    // 16-element units per row
     constexpr int RPU = 32 / UPR;  // rows per warp instruction
-    const int jc = u.c - (kt * C::TN + row0);  // local rows below jc are fp8 cache rows
-#pragma unroll
-    for (int it = 0; it < 32 / RPU; ++it) {
+    for (int it = 0; it * RPU < nrows; ++it) {
       const int lr = it * RPU + lane / UPR;
       const int un = lane % UPR;
       const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr));
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
+      if (!(lr < nrows && ((rowmask >> lr) & 1u))) continue;
       const uint32_t o0 = swz128(row0 + lr, 2 * un, C::TN);
       const uint32_t o1 = swz128(row0 + lr, 2 * un + 1, C::TN);
-      if (lr < jc) {  // widen fp8 to bf16 here
+      if (lr < cache_rows) {  // fp8 cache row: widen to bf16 here
         uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (rp) {
           const uint4 codes = ld_global_nc_v4(rp + un * 16);
@@ -223,59 +232,85 @@ __device__ __forceinline__ void gather_rows(const AttnParams& p, const UnitInfo&
 template <int D, bool FP8>
 __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t base, int n_items) {
   using C = WsCfg<D>;
-  static_assert(C::NS % 2 == 0, "stages alternate between two warp pairs");
+  constexpr int RPW = C::TN / 4;  // key rows per producer warp
+  constexpr int CPW = RPW / 16;   // 16-key chunks per producer warp
+  constexpr uint32_t kChunkBytes = 16 * 128;  // one 64-column block of 16 rows
+  constexpr size_t kCacheElt = FP8 ? 1 : 2;
   const int lane = threadIdx.x & 31;
   const int pw = (threadIdx.x >> 5) - 8;  // 0..3
-  const int pair = pw >> 1, half = pw & 1;
   const bool leader = pw == 0 && lane == 0;
+  if (lane == 0) {
+    tma_prefetch_desc(&p.tm.k_new);
+    tma_prefetch_desc(&p.tm.v_new);
+    if constexpr (!FP8) {
+      tma_prefetch_desc(&p.tm.k_cache);
+      tma_prefetch_desc(&p.tm.v_cache);
+    }
+    if (pw == 0) tma_prefetch_desc(&p.tm.q);
+  }
   uint32_t kv_iter = 0, q_phase = 0;
-  constexpr size_t kCacheElt = FP8 ? 1 : 2;
-  constexpr int RPI = 32 / C::CPR;  // bf16 rows per warp instruction
   for (int k = 0;; ++k) {
     if (leader) ring_put(sh, p, k, n_items);
     const int item = ring_get(sh, k);
     if (item < 0) break;
     const UnitInfo u = decode_item(p, item);
 
-    // ---- Q tiles (zero rows for padding), all four warps ----
-    if (!sh.wait(wsbar::Q_EMPTY, q_phase ^ 1)) break;
-    q_phase ^= 1;
-    for (int i = 0; i < u.nt; ++i) {
-      const uint32_t sQ = base + C::Q_OFF + i * C::Q_BYTES;
-      const int t = u.t0 + i;
+    // ---- Q tiles ----
+    if (pw == 0) {
+      if (!sh.wait(wsbar::Q_EMPTY, q_phase ^ 1)) break;
+      q_phase ^= 1;
+      if (lane == 0) {
+        const uint32_t box_bytes = static_cast<uint32_t>(p.group * p.tq * 128);
+        mbar_arrive_expect_tx(sh.bar(wsbar::Q_FULL), u.nt * (D / 64) * box_bytes);
+        for (int i = 0; i < u.nt; ++i) {
 #pragma unroll
-      for (int it = 0; it < 32 / RPI; ++it) {
-        const int row = 32 * pw + it * RPI + lane / C::CPR;
-        const int ch = lane % C::CPR;
-        const int rt = row / p.group, rh = row % p.group, rj = t * p.tq + rt;
-        const bool v = rt < p.tq && rj < u.n;
-        const char* src =
-            static_cast<const char*>(p.q) +
-            (v ? (((size_t)(u.q_start + rj) * p.num_q_heads + u.g * p.group + rh) * D) * 2 + ch * 16
-               : 0);
-        cp_async_16(sQ + swz128(row, ch, C::M), src, v ? 16u : 0u);
+          for (int db = 0; db < D / 64; ++db)
+            tma_load_3d(base + C::Q_OFF + i * C::Q_BYTES + db * (C::M * 128), &p.tm.q, db * 64,
+                        u.g * p.group, u.q_start + (u.t0 + i) * p.tq, sh.bar(wsbar::Q_FULL));
+        }
       }
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(sh.bar(wsbar::Q_FULL));
 
-    // ---- K/V tiles of the union interval, alternating between the pairs ----
+    // ---- K/V tiles of the union interval ----
     bool ok = true;
     for (int kt = u.lo; kt < u.hi; ++kt, ++kv_iter) {
-      if ((kv_iter & 1) != (uint32_t)pair) continue;
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
       if (!sh.wait(wsbar::KV_EMPTY + 8 * s, ph ^ 1)) { ok = false; break; }
       const uint32_t sK = base + C::KV_OFF + (2 * s) * C::KV_BYTES;
-      const uint32_t sV = sK + C::KV_BYTES;
+      const int row0 = pw * RPW;
+      const int p_row0 = kt * C::TN + row0;  // key position of this warp's first row
+      // chunk classification (lane c < CPW): 1 = cache box, 2 = new-token box, 0 = row gather
+      int ctype = 0, crow = 0;
+      if (lane < CPW) {
+        const int p0 = p_row0 + 16 * lane;
+        if (p0 >= u.c) {
+          ctype = 2;
+          crow = u.q_start + p0 - u.c;
+        } else if (!FP8 && p0 + 15 < u.c) {
+          const int lp = p0 / p.page_size;
+          if ((p0 + 15) / p.page_size == lp) {
+            const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
+            if (page >= 0 && page < p.num_pages) {
+              ctype = 1;
+              crow = page * p.page_size + (p0 - lp * p.page_size);
+            }
+          }
+        }
+      }
+      int types[CPW], rows[CPW];
+      uint32_t fb_mask = 0;
 #pragma unroll
-      for (int sub = 0; sub < C::TN / 64; ++sub) {  // this warp's 32-row blocks
-        const int row0 = (C::TN / 2) * half + 32 * sub;
-        const int pos = kt * C::TN + row0 + lane;
-        const char* kp = nullptr;
-        const char* vp = nullptr;
+      for (int c = 0; c < CPW; ++c) {
+        types[c] = __shfl_sync(0xffffffffu, ctype, c);
+        rows[c] = __shfl_sync(0xffffffffu, crow, c);
+        if (types[c] == 0) fb_mask |= 0xFFFFu << (16 * c);
+      }
+      // per-row sources for the row gather (lane r -> row row0 + r)
+      const char* kp = nullptr;
+      const char* vp = nullptr;
+      if (fb_mask != 0 && lane < RPW) {
+        const int pos = p_row0 + lane;
         if (pos < u.c) {
           const int lp = pos / p.page_size;
           const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -292,14 +327,37 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
           kp = static_cast<const char*>(p.k_new) + off * 2;
           vp = static_cast<const char*>(p.v_new) + off * 2;
         }
-        gather_rows<D, FP8>(p, u, kt, row0, kp, sK);
-        gather_rows<D, FP8>(p, u, kt, row0, vp, sV);
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(sh.bar(wsbar::K_FULL + 8 * s));
-      mbar_arrive(sh.bar(wsbar::V_FULL + 8 * s));
+      const int cache_rows = u.c - p_row0;  // rows below this are cache rows (fp8 widening)
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const uint32_t sX = sK + w * C::KV_BYTES;
+        const uint32_t bar = sh.bar((w == 0 ? wsbar::K_FULL : wsbar::V_FULL) + 8 * s);
+        uint32_t bytes = 0;
+        if (lane == 0) {
+#pragma unroll
+          for (int c = 0; c < CPW; ++c) {
+            if (types[c] == 0) continue;
+            const void* tm = types[c] == 1 ? (w == 0 ? (const void*)&p.tm.k_cache
+                                                     : (const void*)&p.tm.v_cache)
+                                           : (w == 0 ? (const void*)&p.tm.k_new
+                                                     : (const void*)&p.tm.v_new);
+#pragma unroll
+            for (int db = 0; db < D / 64; ++db)
+              tma_load_3d(sX + db * (C::TN * 128) + (row0 + 16 * c) * 128, tm, db * 64, u.g,
+                          rows[c], bar);
+            bytes += (D / 64) * kChunkBytes;
+          }
+        }
+        if (fb_mask != 0) {
+          gather_rows<D, FP8>(p, row0, RPW, fb_mask, cache_rows, w == 0 ? kp : vp, sX);
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+      }
     }
     if (!ok) break;
   }
@@ -616,7 +674,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(512, 1) attn_ws_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__ AttnParams p) {
   using C = WsCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -640,11 +698,11 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const AttnParams p) {
       mbar_init(sh.bar(O_DONE + 8 * s), 1);
       mbar_init(sh.bar(O_EMPTY + 8 * s), 128);
     }
-    mbar_init(sh.bar(Q_FULL), 128);
+    mbar_init(sh.bar(Q_FULL), 1);  // producer warp 0 lane 0, with the TMA byte count
     mbar_init(sh.bar(Q_EMPTY), 1);
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(sh.bar(K_FULL + 8 * s), 64);  // the 64 threads of the pair that owns stage s
-      mbar_init(sh.bar(V_FULL + 8 * s), 64);
+      mbar_init(sh.bar(K_FULL + 8 * s), 4);  // one arrival (with its TMA bytes) per producer warp
+      mbar_init(sh.bar(V_FULL + 8 * s), 4);
       mbar_init(sh.bar(KV_EMPTY + 8 * s), 1);
     }
     mbar_init(sh.bar(FIN), 1);

@@ -2,6 +2,7 @@
 // kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,7 +31,18 @@ struct Stage1Params {
   int32_t* status;
 };
 
+// TMA descriptors of one call (encoded on the host per call; passed as a __grid_constant__
+// kernel parameter so that the kernel can hand their parameter-space address to the TMA unit).
+//   q             [total_q][Hq][D] bf16, box {64, G, tq}: one query tile, token-major rows
+//   k_new, v_new  [total_q][Hkv][D] bf16, box {64, 1, 16}: 16 keys of one KV head
+//   k_cache, v_cache [num_pages * P][Hkv][D] bf16, box {64, 1, 16} (unused for fp8 caches)
+// All use the 128-byte swizzle, matching the operand layout of the MMAs.
+struct TmaMaps {
+  CUtensorMap q, k_new, v_new, k_cache, v_cache;
+};
+
 struct AttnParams {
+  TmaMaps tm;
   const void* q;
   const void* k_new;
   const void* v_new;

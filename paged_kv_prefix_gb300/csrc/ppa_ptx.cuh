@@ -101,6 +101,32 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 }
 
 // ------------------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor) and transaction-counted mbarrier arrivals
+// ------------------------------------------------------------------------------------
+// Arrive once and add `bytes` to the barrier's expected transaction count. The count may run
+// ahead of the expectation (bulk copies completing first): the phase cannot complete before
+// every arrival has happened.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// 3-D tiled TMA load of one box into shared memory at `dst`, completing `bytes` on `bar`.
+// The innermost coordinate times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // Tensor Memory
 // ------------------------------------------------------------------------------------
 // Whole warp: allocate `ncols` (power of two, 32..512) TMEM columns; the base address is
