@@ -130,8 +130,9 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
                       void* out, void* workspace, int32_t* device_status, void* stream);
 
-/* Size of the scratch ppa_prefill_noalloc keeps in a static device array: 2 MiB, enough for
- * about 100,000 query tiles (20 bytes each, plus under 1 KiB of header and padding). */
+/* Size of the scratch ppa_prefill_noalloc keeps in a static device array: 2 MiB. The scratch a
+ * batch needs is ppa_workspace_bytes(): about 32 + 4 * num_kv_heads bytes per query tile plus 16
+ * bytes per sequence, so 2 MiB holds, for example, about 32,000 query tiles at 8 KV heads. */
 #define PPA_NOALLOC_WORKSPACE_BYTES (2u << 20)
 
 /* ppa_prefill for callers that cannot allocate device memory: no workspace argument.

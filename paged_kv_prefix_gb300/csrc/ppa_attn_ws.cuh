@@ -1,9 +1,9 @@
 // Stage 2: a warp-specialised, pipelined attention kernel for sm_103a.
 //
 // One persistent CTA per SM, 16 warps:
-//   warps 0-3   softmax for query tile A (one thread per row)     \ 192 registers each
+//   warps 0-3   softmax for query tile A (one thread per row)     \ 184 registers each
 //   warps 4-7   softmax for query tile B                          /
-//   warps 8-11  producers: TMA / cp.async paged K/V gather and Q   \ 64 registers each
+//   warps 8-11  producers: TMA / cp.async paged K/V gather and Q   \ 72 registers each
 //   warp  12    MMA issue (lane 0)                                  |
 //   warps 13-15 idle                                               /
 // A unit of work is two consecutive 128-row query tiles (tq tokens x G heads each, token
@@ -373,6 +373,12 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   if ((threadIdx.x & 31) != 0) return;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::TN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
+  // Descriptors are built once; a K-step adds a compile-time offset (in 16-byte units) to the
+  // 14-bit start-address field, which cannot carry because shared addresses stay below 256 KB.
+  const uint64_t dQ0 = sdesc_sw128(base + C::Q_OFF, 16, 1024);
+  const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
+  const uint64_t dV0 = sdesc_sw128(base + C::KV_OFF + C::KV_BYTES, C::TN * 128, 1024);
+  constexpr uint32_t kQStep = C::Q_BYTES >> 4, kStageStep = (2 * C::KV_BYTES) >> 4;
   uint32_t kv_iter = 0, q_phase = 0;
   uint32_t pf_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
   bool ok = true;
@@ -384,15 +390,13 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     q_phase ^= 1;
     tc_fence_after();
     auto issue_s = [&](int i, int stage) {
-      const uint32_t sQ = base + C::Q_OFF + i * C::Q_BYTES;
-      const uint32_t sK = base + C::KV_OFF + (2 * stage) * C::KV_BYTES;
       const uint32_t tS = tmem + C::TM_S + i * C::TN;
+      const uint64_t a0 = dQ0 + i * kQStep, b0 = dK0 + stage * kStageStep;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t db = kk >> 2, ks = kk & 3;
-        mma_bf16_ss(tS, sdesc_sw128(sQ + db * (C::M * 128) + ks * 32, 16, 1024),
-                    sdesc_sw128(sK + db * (C::TN * 128) + ks * 32, 16, 1024), kIdescS,
-                    kk > 0 ? 1u : 0u);
+        const uint32_t off_a = ((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4;
+        const uint32_t off_b = ((kk >> 2) * (C::TN * 128) + (kk & 3) * 32) >> 4;
+        mma_bf16_ss(tS, a0 + off_a, b0 + off_b, kIdescS, kk > 0 ? 1u : 0u);
       }
       tc_commit(sh.bar(wsbar::S_FULL + 8 * i));
     };
@@ -416,14 +420,13 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         pf_phase[i] ^= 1;
         if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t sV = base + C::KV_OFF + (2 * s + 1) * C::KV_BYTES;
         const uint32_t tP = tmem + C::TM_S + i * C::TN;
         const uint32_t tO = tmem + C::TM_O + i * D;
+        const uint64_t b0 = dV0 + s * kStageStep;
+        const uint32_t acc0 = kt > u.lo_i[i] ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < C::TN / 16; ++kk) {
-          mma_bf16_ts(tO, tP + kk * 8, sdesc_sw128(sV + kk * 16 * 128, C::TN * 128, 1024),
-                      kIdescO, (kt > u.lo_i[i] || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::TN / 16; ++kk)
+          mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
         if (kt + 1 < u.hi_i[i]) {
           const int s2 = (kv_iter + 1) % C::NS;
           const uint32_t ph2 = ((kv_iter + 1) / C::NS) & 1;
@@ -452,16 +455,18 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::TN, false, false);
   constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
   uint32_t kv_iter = 0, q_phase = 0, pf_phase = 0, oe_phase = 0, sc = 0;
-  const uint32_t sQ = base + C::Q_OFF;
+  const uint64_t dQ = sdesc_sw128(base + C::Q_OFF, 16, 1024);
+  const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
+  const uint64_t dV0 = sdesc_sw128(base + C::KV_OFF + C::KV_BYTES, C::TN * 128, 1024);
+  constexpr uint32_t kStageStep = (2 * C::KV_BYTES) >> 4;
   auto issue_s = [&](int stage, uint32_t buf) {
-    const uint32_t sK = base + C::KV_OFF + (2 * stage) * C::KV_BYTES;
     const uint32_t tS = tmem + C::TM_S + buf * C::TN;
+    const uint64_t b0 = dK0 + stage * kStageStep;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t db = kk >> 2, ks = kk & 3;
-      mma_bf16_ss(tS, sdesc_sw128(sQ + db * (C::M * 128) + ks * 32, 16, 1024),
-                  sdesc_sw128(sK + db * (C::TN * 128) + ks * 32, 16, 1024), kIdescS,
-                  kk > 0 ? 1u : 0u);
+      const uint32_t off_a = ((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4;
+      const uint32_t off_b = ((kk >> 2) * (C::TN * 128) + (kk & 3) * 32) >> 4;
+      mma_bf16_ss(tS, dQ + off_a, b0 + off_b, kIdescS, kk > 0 ? 1u : 0u);
     }
     tc_commit(sh.bar(wsbar::S_FULL + 8 * buf));
   };
@@ -495,14 +500,13 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
       pf_phase ^= 1;
       if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sV = base + C::KV_OFF + (2 * s + 1) * C::KV_BYTES;
       const uint32_t tP = tmem + C::TM_S + (sc & 1) * C::TN;
+      const uint64_t b0 = dV0 + s * kStageStep;
+      const uint32_t acc0 = kt > u.lo ? 1u : 0u;
 #pragma unroll
-      for (int kk = 0; kk < C::TN / 16; ++kk) {
-        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8,
-                    sdesc_sw128(sV + kk * 16 * 128, C::TN * 128, 1024), kIdescO,
-                    (kt > u.lo || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < C::TN / 16; ++kk)
+        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
+                    kk > 0 ? 1u : acc0);
       tc_commit(sh.bar(wsbar::O_DONE));
       tc_commit(sh.bar(wsbar::KV_EMPTY + 8 * s));
       ++kv_iter;
@@ -720,10 +724,10 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
   const int n_items = p.ws->n_items;
 
   if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
     ws_softmax<D, FP8>(p, sh, tmem);
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp < 12) {
       ws_producer<D, FP8>(p, sh, base, n_items);
     } else if (warp == 12) {
