@@ -100,12 +100,19 @@ struct WsShared {
   }
 };
 
+// Bounded wait by a whole warp with a warp-uniform outcome (a lane that gives up makes every
+// lane give up, so the warp never splits around later warp-collective operations).
+__device__ __forceinline__ bool wait_warp(const WsShared& sh, int off, uint32_t parity) {
+  const bool ok = sh.wait(off, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Consumer side of the item ring (whole warp): the k-th item of this CTA, or -1 at the end.
 __device__ __forceinline__ int ring_get(const WsShared& sh, int k) {
   const int slot = k & 1;
   int item = -1;
   if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
-  __syncwarp();
+  item = __shfl_sync(0xffffffffu, item, 0);  // one outcome for the whole warp
   if ((threadIdx.x & 31) == 0) mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
   return item;
 }
@@ -155,6 +162,14 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   u.hi_i[1] = un.nt > 1 ? un.hi1 : 0;
   u.lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
   u.hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
+  return u;
+}
+
+// The same unit in every lane, taken from lane 0, so the compiler can keep it warp-uniform.
+__device__ __forceinline__ UnitInfo uniform_unit(UnitInfo u) {
+  int* f = reinterpret_cast<int*>(&u);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(UnitInfo) / sizeof(int)); ++i) f[i] = __shfl_sync(0xffffffffu, f[i], 0);
   return u;
 }
 
@@ -257,7 +272,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
 
     // ---- Q tiles ----
     if (pw == 0) {
-      if (!sh.wait(wsbar::Q_EMPTY, q_phase ^ 1)) break;
+      if (!wait_warp(sh, wsbar::Q_EMPTY, q_phase ^ 1)) break;
       q_phase ^= 1;
       if (lane == 0) {
         const uint32_t box_bytes = static_cast<uint32_t>(p.group * p.tq * 128);
@@ -276,7 +291,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
     for (int kt = u.lo; kt < u.hi; ++kt, ++kv_iter) {
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
-      if (!sh.wait(wsbar::KV_EMPTY + 8 * s, ph ^ 1)) { ok = false; break; }
+      if (!wait_warp(sh, wsbar::KV_EMPTY + 8 * s, ph ^ 1)) { ok = false; break; }
       const uint32_t sK = base + C::KV_OFF + (2 * s) * C::KV_BYTES;
       const int row0 = pw * RPW;
       const int p_row0 = kt * C::TN + row0;  // key position of this warp's first row
@@ -558,10 +573,10 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       const uint32_t buf = C::NQ == 2 ? 0u : (sc & 1);
       const uint32_t tS = tmem + C::TM_S + (i * C::NSB + buf) * C::TN + lane_off;
       if constexpr (C::NQ == 2) {
-        if (!sh.wait(wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
+        if (!wait_warp(sh, wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
         sf_phase ^= 1;
       } else {
-        if (!sh.wait(wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
+        if (!wait_warp(sh, wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
       }
       ++sc;
       tc_fence_after();
@@ -629,7 +644,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       // in order). NQ == 1: S(kt) was issued before PV(kt-1), so wait for that PV first.
       if constexpr (C::NQ == 1) {
         if (kt > lo) {
-          if (!sh.wait(wsbar::O_DONE, od_phase)) { ok = false; break; }
+          if (!wait_warp(sh, wsbar::O_DONE, od_phase)) { ok = false; break; }
           od_phase ^= 1;
           tc_fence_after();
         }
@@ -650,7 +665,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     }
     if (!ok) break;
     // ---- epilogue: the last PV of this tile ----
-    if (!sh.wait(wsbar::O_DONE + 8 * i, od_phase)) break;
+    if (!wait_warp(sh, wsbar::O_DONE + 8 * i, od_phase)) break;
     od_phase ^= 1;
     tc_fence_after();
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
