@@ -599,13 +599,20 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
 #pragma unroll
         for (int e = 0; e < C::TN; ++e) sv[e] = (e < a0 || e > a1) ? neg_inf : sv[e];
       }
+      // row maximum: 8 independent chains of 3-input maxima over columns q, q+8, q+16, ...
+      constexpr int kPer = C::TN / 8;
       float mx[8];
 #pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) mx[q8] = sv[q8];
+      for (int q8 = 0; q8 < 8; ++q8) {
+        float m = fmax3(sv[q8], sv[q8 + 8], sv[q8 + 16]);
+        int jj = 3;
 #pragma unroll
-      for (int e = 8; e < C::TN; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+        for (; jj + 1 < kPer; jj += 2) m = fmax3(m, sv[q8 + 8 * jj], sv[q8 + 8 * jj + 8]);
+        if (jj < kPer) m = fmaxf(m, sv[q8 + 8 * jj]);
+        mx[q8] = m;
+      }
       const float tile_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_tile = tile_max * scale;  // in exp2 units
       // Keep the stale reference unless the maximum grew by more than 2^8.
       bool rescale = false;
@@ -616,13 +623,17 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         m_ref = m_tile;
       }
       const float m_use = m_ref == neg_inf ? 0.f : m_ref;
-      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // p = exp2(s * scale - m): the exponent arguments and the row sums run as packed pairs
+      const uint64_t scale2 = f2_pack(scale, scale), negm2 = f2_pack(-m_use, -m_use);
+      uint64_t sum2[4] = {0, 0, 0, 0};
       uint32_t pk[C::TN / 2];
 #pragma unroll
       for (int e = 0; e < C::TN; e += 2) {
-        float p0 = ex2_approx(fmaf(sv[e], scale, -m_use));
-        float p1 = ex2_approx(fmaf(sv[e + 1], scale, -m_use));
-        sum[(e >> 1) & 7] += p0 + p1;
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(sv[e], sv[e + 1]), scale2, negm2), y0, y1);
+        float p0 = ex2_approx(y0);
+        float p1 = ex2_approx(y1);
+        sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
         if constexpr (FP8) {
           const int jc = min(max(u.c - k0, 0), C::TN);
           p0 = e < jc ? p0 * vs_ctx : p0;
@@ -630,8 +641,11 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         }
         pk[e >> 1] = pack_bf16x2(p0, p1);
       }
+      float sl[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) f2_unpack(sum2[q4], sl[2 * q4], sl[2 * q4 + 1]);
       l_run = l_run * alpha +
-              (((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+              (((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7])));
       // P over the first TN/2 columns of this S buffer
 #pragma unroll
       for (int cc = 0; cc < C::TN / 64; ++cc) {
