@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload nonpow2|swa64|swa1024|mm|mixed] [--no-cpu-baseline]
+                    [--sweep windows]
 
 A step is one pass of the whole hot path over one batch: for every shape of the workload,
 stage 1 (live key-tile bounds and work list) and the attention kernel, through the C ABI.
@@ -96,10 +97,51 @@ def recorded_traffic(workload: str):
     return ent.get("dram_bytes_per_launch")
 
 
+def algorithmic_flops(binding, dc, case, stream) -> float:
+    """4 * D * Hq per live (query, key) pair: QK^T and PV, 2*D each, per query head."""
+    import torch
+    cnt = torch.zeros(1, dtype=torch.int64, device=dc.q.device)
+    binding.ppa_live_pairs(dc.dims, dc.cu_query_lens, dc.context_lens, dc.mm_ranges, cnt, stream)
+    return 4.0 * case.head_dim * case.num_q_heads * float(cnt.item())
+
+
+def algorithmic_bytes(binding, dc, case, stream) -> float:
+    """Bytes one pass must move at least once: Q and O, k_new and v_new, every live cached
+    token's K and V row once per KV head, the block-table entries read and the ranges."""
+    import torch
+    cnt = torch.zeros(1, dtype=torch.int64, device=dc.q.device)
+    binding.ppa_live_kv_tokens(dc.dims, dc.cu_query_lens, dc.context_lens, dc.mm_ranges, cnt,
+                               stream)
+    D, Hq, Hkv = case.head_dim, case.num_q_heads, case.num_kv_heads
+    kv_bytes = 1 if case.kv_dtype == "fp8_e4m3" else 2
+    ctx = case.context_lens.numpy().astype(np.int64)
+    table = int(((ctx + case.page_size - 1) // case.page_size).sum()) * 4
+    ranges = 0 if case.mm_ranges is None else case.mm_ranges.numel() * 4
+    return (case.total_q * (2 * Hq * D + 2 * Hkv * D) * 2
+            + float(cnt.item()) * 2 * Hkv * D * kv_bytes + table + ranges)
+
+
+def roofline(flops: float, nbytes: float, seconds: float, peaks: dict, peak_src: str) -> dict:
+    """The bound of one launch: tensor cores when its intensity is above the ridge of the
+    measured peaks, HBM below it."""
+    tflops_peak = float(peaks["bf16_tflops"])
+    gbs_peak = float(peaks["hbm_gbs"])
+    ridge = tflops_peak * 1e12 / (gbs_peak * 1e9)
+    intensity = flops / max(nbytes, 1.0)
+    if intensity >= ridge:
+        a = flops / seconds / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": tflops_peak, "unit": "TFLOP/s",
+                "frac": a / tflops_peak, "intensity_flop_per_byte": intensity,
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+    a = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": a, "peak": gbs_peak, "unit": "GB/s", "frac": a / gbs_peak,
+            "intensity_flop_per_byte": intensity, "peak_source": f"{peak_src} HBM copy"}
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -113,7 +155,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -123,7 +165,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -137,16 +185,21 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        t0, t1 = getattr(self, "t0", 0.0), getattr(self, "t1", float("inf"))
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1 + 0.05]
+        if not inside and self.lines:  # timed region shorter than the sampling period
+            mid = 0.5 * (t0 + min(t1, self.lines[-1][0]))
+            inside = [min(self.lines, key=lambda x: abs(x[0] - mid))[1]]
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[4:8]):
+            for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": float(np.median(sm)) if sm else None,
@@ -273,13 +326,12 @@ def run_ours(args):
     dcs = [binding.DeviceCase(c, device=dev) for c in cases]
     stream = torch.cuda.current_stream(dev)
 
-    # live pairs and FLOPs, from the library's interval arithmetic
-    flops, tokens = [], 0
+    # live pairs and FLOPs, live cache tokens and algorithmic bytes, from the library's own
+    # interval arithmetic
+    flops, nbytes, tokens = [], [], 0
     for dc, case in zip(dcs, cases):
-        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
-        binding.ppa_live_pairs(dc.dims, dc.cu_query_lens, dc.context_lens, dc.mm_ranges, cnt,
-                               stream)
-        flops.append(4.0 * case.head_dim * case.num_q_heads * float(cnt.item()))
+        flops.append(algorithmic_flops(binding, dc, case, stream))
+        nbytes.append(algorithmic_bytes(binding, dc, case, stream))
         tokens += case.total_q
     step_flops = sum(flops)
 
@@ -294,6 +346,10 @@ def run_ours(args):
             ev_list[i][2].record(stream)
 
     mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in dcs]
+    # clocks: the sampler runs from before the warm-up; samples inside the timed region count
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
     for _ in range(args.warmup):
         flush.zero_()
         step(mk())
@@ -304,12 +360,11 @@ def run_ours(args):
             raise SystemExit(f"device status {st}: {binding.status_string(st)}")
 
     events = [mk() for _ in range(args.steps)]
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
-        sampler.start()
+        sampler.mark(True)
     t_wall = time.perf_counter()
     for k in range(args.steps):
         flush.zero_()
@@ -318,6 +373,8 @@ def run_ours(args):
     t_wall = time.perf_counter() - t_wall
     if dist is not None:
         dist.barrier()
+    if sampler:
+        sampler.mark(False)
     clocks = sampler.stop() if sampler else None
 
     step_ms = [sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(len(dcs))) for ev in events]
@@ -347,15 +404,19 @@ def run_ours(args):
     shape_tot = attend_ms.sum(axis=0)
     dom = int(np.argmax(shape_tot))
     dom_avg_s = float(attend_ms[:, dom].mean()) * 1e-3
-    achieved = flops[dom] / dom_avg_s / 1e12
     peak = float(peaks["bf16_tflops"])
+    roof = roofline(flops[dom], nbytes[dom], dom_avg_s, peaks, peak_src)
+    roof["traffic"] = recorded_traffic(args.workload)
+    roof["kernel"] = f"attn_ws_kernel ({cases[dom].name})"
     shapes = []
     for i, case in enumerate(cases):
         a = float(attend_ms[:, i].mean())
         shapes.append({"shape": case.name, "attend_ms": round(a, 4),
                        "plan_ms": round(float(plan_ms[:, i].mean()), 4),
                        "tflops": round(flops[i] / (a * 1e-3) / 1e12, 2),
-                       "live_tflop": round(flops[i] / 1e12, 4)})
+                       "gbs": round(nbytes[i] / (a * 1e-3) / 1e9, 1),
+                       "live_tflop": round(flops[i] / 1e12, 4),
+                       "algorithmic_mb": round(nbytes[i] / 1e6, 2)})
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         f, s, sample = oracle_sample(cases, args.cpu_seconds)
@@ -378,10 +439,7 @@ def run_ours(args):
                    "seed_per_rank": "rank"},
         "pct_bf16_peak": 100.0 * value / peak,
         "tokens_per_s": all_tokens / (total_ms * 1e-3),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
-                     "kernel": f"attn_kernel ({cases[dom].name})",
-                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "roofline": roof,
         "shapes": shapes,
         "e2e": e2e,
         "gpu_launches": 2 * len(dcs) * args.steps,
@@ -443,6 +501,44 @@ def run_e2e(args, cases, dcs, step_flops, stream, dev):
             "ms_per_step": ms}
 
 
+def run_window_sweep(args):
+    """Causal sliding-window prefill over a grid of sequence lengths and windows: time should
+    follow the live pairs (~ L * W), not L^2. One JSON line per point."""
+    import torch
+    from paged_kv_prefix_gb300 import binding
+    from paged_kv_prefix_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for seq_len in (16384, 32768, 65536):
+        for window in (512, 1024, 2048):
+            case = wl.swa_causal(seed=0, seq_len=seq_len, window=window)
+            dc = binding.DeviceCase(case)
+            flops = algorithmic_flops(binding, dc, case, stream)
+            nbytes = algorithmic_bytes(binding, dc, case, stream)
+            dc.plan(stream)
+            ms = []
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dc.attend(stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if k >= args.warmup:
+                    ms.append(e0.elapsed_time(e1))
+            st = dc.read_status(stream)
+            t = float(np.median(ms)) * 1e-3
+            print(json.dumps({"sweep": "sliding_window_causal", "seq_len": seq_len, "window": window,
+                              "attend_ms": t * 1e3, "live_pairs_per_head": flops / (4 * 64 * 8),
+                              "tflops": flops / t / 1e12, "gbs": nbytes / t / 1e9,
+                              "ns_per_mpair": t * 1e9 / (flops / (4 * 64 * 8) / 1e6),
+                              "roofline": roofline(flops, nbytes, t, peaks, peak_src),
+                              "status": st}), flush=True)
+            del dc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,10 +549,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--sweep", choices=["windows"], default=None,
+                    help="print one line per point of a window / length sweep instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.sweep == "windows":
+        run_window_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

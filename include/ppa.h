@@ -183,6 +183,14 @@ ppa_status ppa_live_pairs(const ppa_dims* dims, const int32_t* cu_query_lens,
                           const int32_t* context_lens, const int32_t* mm_ranges,
                           unsigned long long* count_out, void* stream);
 
+/* Number of cached context tokens (positions k < c) that at least one query of their sequence
+ * may attend to, summed over the batch, written to the device uint64 *count_out. These are
+ * the cache rows one prefill pass must read at least once (one KV head); the algorithmic HBM
+ * bytes of a pass count each of them once per KV head for K and for V. */
+ppa_status ppa_live_kv_tokens(const ppa_dims* dims, const int32_t* cu_query_lens,
+                              const int32_t* context_lens, const int32_t* mm_ranges,
+                              unsigned long long* count_out, void* stream);
+
 /* Testing: decodes n fp8 e4m3fn codes to bf16 bit patterns with the attention kernel's own
  * conversion (exact; NaN codes give a bf16 NaN). */
 ppa_status ppa_debug_e4m3_to_bf16(const uint8_t* codes, uint16_t* bf16_out, int n, void* stream);

@@ -70,6 +70,7 @@ _SIGNATURES = {
     "ppa_tile_bounds": (_I, [_DIMS, _I, _I, _P, _P, _P, _P, _P, _P]),
     "ppa_debug_mask": (_I, [_DIMS, _I, _P, _P, _P, _P, _I, _I, _P]),
     "ppa_live_pairs": (_I, [_DIMS, _P, _P, _P, _P, _P]),
+    "ppa_live_kv_tokens": (_I, [_DIMS, _P, _P, _P, _P, _P]),
     "ppa_debug_e4m3_to_bf16": (_I, [_P, _P, _I, _P]),
     "ppa_read_status": (_I, [_P, _P]),
     "ppa_status_string": (ctypes.c_char_p, [_I]),
@@ -213,6 +214,15 @@ def ppa_live_pairs(dims: PpaDims, cu_query_lens, context_lens, mm_ranges, count_
                                 _ptr(mm_ranges), _ptr(count_out), _stream(stream))
     if check:
         _check(code, "ppa_live_pairs")
+    return code
+
+
+def ppa_live_kv_tokens(dims: PpaDims, cu_query_lens, context_lens, mm_ranges, count_out,
+                       stream=None, check: bool = True) -> int:
+    code = lib().ppa_live_kv_tokens(ctypes.byref(dims), _ptr(cu_query_lens), _ptr(context_lens),
+                                    _ptr(mm_ranges), _ptr(count_out), _stream(stream))
+    if check:
+        _check(code, "ppa_live_kv_tokens")
     return code
 
 

@@ -331,6 +331,21 @@ ppa_status ppa_live_pairs(const ppa_dims* dims, const int32_t* cu_query_lens,
              : PPA_ERR_CUDA;
 }
 
+ppa_status ppa_live_kv_tokens(const ppa_dims* dims, const int32_t* cu_query_lens,
+                              const int32_t* context_lens, const int32_t* mm_ranges,
+                              unsigned long long* count_out, void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (cu_query_lens == nullptr || context_lens == nullptr || count_out == nullptr)
+    return PPA_ERR_INVALID;
+  if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
+  return ppa::launch_live_kv_tokens(mask_of(dims, mm_ranges), dims->num_seqs, cu_query_lens,
+                                    context_lens, count_out,
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
+}
+
 ppa_status ppa_debug_e4m3_to_bf16(const uint8_t* codes, uint16_t* bf16_out, int n, void* stream) {
   if (n < 0 || (n > 0 && (codes == nullptr || bf16_out == nullptr))) return PPA_ERR_INVALID;
   return ppa::launch_e4m3_decode(codes, bf16_out, n, static_cast<cudaStream_t>(stream)) ==

@@ -74,6 +74,9 @@ cudaError_t launch_debug_mask(const MaskParams& mp, int seq, const int32_t* cu, 
                               cudaStream_t stream);
 cudaError_t launch_live_pairs(const MaskParams& mp, int num_seqs, int total_q, const int32_t* cu,
                               const int32_t* ctx, unsigned long long* out, cudaStream_t stream);
+cudaError_t launch_live_kv_tokens(const MaskParams& mp, int num_seqs, const int32_t* cu,
+                                  const int32_t* ctx, unsigned long long* out,
+                                  cudaStream_t stream);
 cudaError_t launch_e4m3_decode(const uint8_t* codes, uint16_t* out, int n, cudaStream_t stream);
 
 // Attention kernels, one translation unit per head dimension. `max_ctas` bounds the

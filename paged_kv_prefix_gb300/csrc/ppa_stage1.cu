@@ -314,6 +314,38 @@ __global__ void live_pairs_kernel(const MaskParams mp, int num_seqs, int total_q
   if ((threadIdx.x & 31) == 0 && acc) atomicAdd(out, acc);
 }
 
+// One CTA per sequence: the cached context keys that at least one of its queries may attend
+// to. The union of the rows' allowed intervals is itself an interval (each row's contains the
+// row's own position and the positions are consecutive), so it is [min kmin, max kmax].
+__global__ void live_kv_tokens_kernel(const MaskParams mp, const int32_t* cu, const int32_t* ctx,
+                                      unsigned long long* out) {
+  __shared__ int s_lo[32], s_hi[32];
+  const int b = blockIdx.x;
+  const int c = ctx[b];
+  const int n = cu[b + 1] - cu[b];
+  const int32_t* ranges = mp.mm_ranges ? mp.mm_ranges + (size_t)b * mp.max_mm_ranges * 2 : nullptr;
+  int lo = INT_MAX, hi = INT_MIN;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    int kmin, kmax;
+    row_interval(c + j, c + n, mp, ranges, kmin, kmax);
+    lo = min(lo, kmin);
+    hi = max(hi, kmax);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_down_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_down_sync(0xffffffffu, hi, o));
+  }
+  const int warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if ((threadIdx.x & 31) == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; ++w) { lo = min(lo, s_lo[w]); hi = max(hi, s_hi[w]); }
+    const int top = min(hi, c - 1);
+    if (n > 0 && top >= lo) atomicAdd(out, (unsigned long long)(top - lo + 1));
+  }
+}
+
 __global__ void e4m3_decode_kernel(const uint8_t* codes, uint16_t* out, int n) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (i >= n) return;
@@ -351,6 +383,16 @@ cudaError_t launch_live_pairs(const MaskParams& mp, int num_seqs, int total_q, c
   if (total_q == 0 || num_seqs == 0) return cudaSuccess;
   const int grid = min(1184, (total_q + 255) / 256);
   live_pairs_kernel<<<grid, 256, 0, stream>>>(mp, num_seqs, total_q, cu, ctx, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_live_kv_tokens(const MaskParams& mp, int num_seqs, const int32_t* cu,
+                                  const int32_t* ctx, unsigned long long* out,
+                                  cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  if (num_seqs == 0) return cudaSuccess;
+  live_kv_tokens_kernel<<<num_seqs, 256, 0, stream>>>(mp, cu, ctx, out);
   return cudaGetLastError();
 }
 

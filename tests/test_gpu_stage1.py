@@ -117,3 +117,23 @@ def test_e4m3_decode_bit_exact():
     out2 = torch.zeros(7, dtype=torch.int16, device="cuda")
     binding.ppa_debug_e4m3_to_bf16(codes[100:107], out2, 7)
     assert np.array_equal(out2.view(torch.bfloat16).float().cpu().numpy(), table[100:107])
+
+
+@pytest.mark.parametrize("case", _geometry_cases()[:12], ids=lambda c: c.name)
+def test_live_kv_tokens_bit_exact(case):
+    """Cached context keys that some query of the sequence may attend to, from the dense mask."""
+    inp = case.numpy_inputs()
+    want = 0
+    for b in range(case.num_seqs):
+        c = int(inp["context_lens"][b])
+        n = int(inp["cu_query_lens"][b + 1] - inp["cu_query_lens"][b])
+        if n == 0 or c == 0:
+            continue
+        m = ref.allowed_mask(c + np.arange(n), c + n, case.causal, case.window_left,
+                             case.window_right, None if inp["mm_ranges"] is None
+                             else inp["mm_ranges"][b], case.clamp_mm)
+        want += int(m[:, :c].any(axis=0).sum())
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    binding.ppa_live_kv_tokens(binding.dims_for(case), case.cu_query_lens.cuda(),
+                               case.context_lens.cuda(), _dev(case.mm_ranges), out)
+    assert int(out.item()) == want
