@@ -72,8 +72,9 @@ struct WsCfg {
 // Barrier and slot offsets inside the barrier block.
 namespace wsbar {
 constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL = 48,
-              V_FULL = 80, KV_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
-              O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224;
+              V_FULL = 80, K_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
+              O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224,
+              V_EMPTY = 240;
 constexpr int kRingConsumers = 13;  // warps 0..12 each release a ring slot once
 }  // namespace wsbar
 
@@ -182,14 +183,16 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 //
 // Q: producer warp 0 loads each query tile with one TMA box per 64-column block; the box
 // {64 columns, G heads, tq tokens} lands as token-major rows, exactly the MMA's A operand.
-// K/V: every producer warp owns a quarter of each key tile (TN/4 rows = one or two chunks of
-// 16 keys). A chunk whose 16 keys are cached context in one page, or are all new tokens, is one
-// TMA box per 64-column block from the cache or the k_new/v_new tensor (rows past the
-// sequence read the next sequence's tokens or the zero fill beyond the tensor: finite values
-// that the mask removes). Any other chunk (it straddles the context end or a page boundary;
-// the page id is out of range; the cache is fp8 and must be widened) is gathered row by row
-// with cp.async, as the PR #54194 report describes for per-token offsets. Each warp then
-// arrives once on k_full / v_full with the byte count of its boxes.
+// K/V: warps 0-1 stream K and warps 2-3 stream V, each owning half of every key tile, with
+// separate empty barriers: a K slot frees as soon as the S MMAs that read it are issued, a V
+// slot after its PV, so K runs up to two tiles ahead of V. A chunk of 16 keys that are cached
+// context in one page, or are all new tokens, is one TMA box per 64-column block from the
+// cache or the k_new/v_new tensor (rows past the sequence read the next sequence's tokens or
+// the zero fill beyond the tensor: finite values that the mask removes). Any other chunk (it
+// straddles the context end or a page boundary; the page id is out of range; the cache is fp8
+// and must be widened) is gathered row by row with cp.async, as the PR #54194 report describes
+// for per-token offsets. Each warp then arrives once on k_full / v_full with the byte count of
+// its boxes.
 // ---------------------------------------------------------------------------------------
 
 // Row-wise gather of rows row0 .. row0+nrows-1 whose bit is set in `rowmask`; `mine` is the
@@ -247,22 +250,26 @@ __device__ __forceinline__ void gather_rows(const AttnParams& p, int row0, int n
 template <int D, bool FP8>
 __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t base, int n_items) {
   using C = WsCfg<D>;
-  constexpr int RPW = C::TN / 4;  // key rows per producer warp
-  constexpr int CPW = RPW / 16;   // 16-key chunks per producer warp
+  constexpr int RPW = C::TN / 2;   // key rows per producer warp (two warps per stream)
+  constexpr int NSUB = RPW / 32;   // 32-row blocks per warp
   constexpr uint32_t kChunkBytes = 16 * 128;  // one 64-column block of 16 rows
   constexpr size_t kCacheElt = FP8 ? 1 : 2;
   const int lane = threadIdx.x & 31;
   const int pw = (threadIdx.x >> 5) - 8;  // 0..3
+  const int w = pw >> 1;                  // 0: the K stream, 1: the V stream
+  const int half = pw & 1;
   const bool leader = pw == 0 && lane == 0;
+  const void* tm_new = w == 0 ? (const void*)&p.tm.k_new : (const void*)&p.tm.v_new;
+  const void* tm_cache = w == 0 ? (const void*)&p.tm.k_cache : (const void*)&p.tm.v_cache;
+  const char* g_cache = static_cast<const char*>(w == 0 ? p.k_cache : p.v_cache);
+  const char* g_new = static_cast<const char*>(w == 0 ? p.k_new : p.v_new);
   if (lane == 0) {
-    tma_prefetch_desc(&p.tm.k_new);
-    tma_prefetch_desc(&p.tm.v_new);
-    if constexpr (!FP8) {
-      tma_prefetch_desc(&p.tm.k_cache);
-      tma_prefetch_desc(&p.tm.v_cache);
-    }
+    tma_prefetch_desc(tm_new);
+    if constexpr (!FP8) tma_prefetch_desc(tm_cache);
     if (pw == 0) tma_prefetch_desc(&p.tm.q);
   }
+  const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
+  const int full_bar = w == 0 ? wsbar::K_FULL : wsbar::V_FULL;
   uint32_t kv_iter = 0, q_phase = 0;
   for (int k = 0;; ++k) {
     if (leader) ring_put(sh, p, k, n_items);
@@ -286,93 +293,84 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       }
     }
 
-    // ---- K/V tiles of the union interval ----
+    // ---- this warp's rows of the K (or V) tiles of the union interval ----
     bool ok = true;
     for (int kt = u.lo; kt < u.hi; ++kt, ++kv_iter) {
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
-      if (!wait_warp(sh, wsbar::KV_EMPTY + 8 * s, ph ^ 1)) { ok = false; break; }
-      const uint32_t sK = base + C::KV_OFF + (2 * s) * C::KV_BYTES;
-      const int row0 = pw * RPW;
-      const int p_row0 = kt * C::TN + row0;  // key position of this warp's first row
-      // chunk classification (lane c < CPW): 1 = cache box, 2 = new-token box, 0 = row gather
-      int ctype = 0, crow = 0;
-      if (lane < CPW) {
-        const int p0 = p_row0 + 16 * lane;
-        if (p0 >= u.c) {
-          ctype = 2;
-          crow = u.q_start + p0 - u.c;
-        } else if (!FP8 && p0 + 15 < u.c) {
-          const int lp = p0 / p.page_size;
-          if ((p0 + 15) / p.page_size == lp) {
-            const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
-            if (page >= 0 && page < p.num_pages) {
-              ctype = 1;
-              crow = page * p.page_size + (p0 - lp * p.page_size);
+      if (!wait_warp(sh, empty_bar + 8 * s, ph ^ 1)) { ok = false; break; }
+      const uint32_t sX = base + C::KV_OFF + (2 * s + w) * C::KV_BYTES;
+      const uint32_t bar = sh.bar(full_bar + 8 * s);
+      uint32_t bytes = 0;
+      bool any_fallback = false;
+#pragma unroll
+      for (int sub = 0; sub < NSUB; ++sub) {
+        const int row0 = half * RPW + 32 * sub;
+        const int p_row0 = kt * C::TN + row0;  // key position of this block's first row
+        // chunk classification (lane c < 2): 1 = cache box, 2 = new-token box, 0 = row gather
+        int ctype = 0, crow = 0;
+        if (lane < 2) {
+          const int p0 = p_row0 + 16 * lane;
+          if (p0 >= u.c) {
+            ctype = 2;
+            crow = u.q_start + p0 - u.c;
+          } else if (!FP8 && p0 + 15 < u.c) {
+            const int lp = p0 / p.page_size;
+            if ((p0 + 15) / p.page_size == lp) {
+              const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
+              if (page >= 0 && page < p.num_pages) {
+                ctype = 1;
+                crow = page * p.page_size + (p0 - lp * p.page_size);
+              }
             }
           }
         }
-      }
-      int types[CPW], rows[CPW];
-      uint32_t fb_mask = 0;
+        int types[2], rows[2];
+        uint32_t fb_mask = 0;
 #pragma unroll
-      for (int c = 0; c < CPW; ++c) {
-        types[c] = __shfl_sync(0xffffffffu, ctype, c);
-        rows[c] = __shfl_sync(0xffffffffu, crow, c);
-        if (types[c] == 0) fb_mask |= 0xFFFFu << (16 * c);
-      }
-      // per-row sources for the row gather (lane r -> row row0 + r)
-      const char* kp = nullptr;
-      const char* vp = nullptr;
-      if (fb_mask != 0 && lane < RPW) {
-        const int pos = p_row0 + lane;
-        if (pos < u.c) {
-          const int lp = pos / p.page_size;
-          const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
-          if (page >= 0 && page < p.num_pages) {
-            const size_t off =
-                (((size_t)page * p.page_size + (pos - lp * p.page_size)) * p.num_kv_heads + u.g) * D;
-            kp = static_cast<const char*>(p.k_cache) + off * kCacheElt;
-            vp = static_cast<const char*>(p.v_cache) + off * kCacheElt;
-          } else {
-            report(p.status, PPA_ERR_BAD_PAGE);
-          }
-        } else if (pos < u.s) {
-          const size_t off = ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D;
-          kp = static_cast<const char*>(p.k_new) + off * 2;
-          vp = static_cast<const char*>(p.v_new) + off * 2;
+        for (int c = 0; c < 2; ++c) {
+          types[c] = __shfl_sync(0xffffffffu, ctype, c);
+          rows[c] = __shfl_sync(0xffffffffu, crow, c);
+          if (types[c] == 0) fb_mask |= 0xFFFFu << (16 * c);
         }
-      }
-      const int cache_rows = u.c - p_row0;  // rows below this are cache rows (fp8 widening)
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const uint32_t sX = sK + w * C::KV_BYTES;
-        const uint32_t bar = sh.bar((w == 0 ? wsbar::K_FULL : wsbar::V_FULL) + 8 * s);
-        uint32_t bytes = 0;
         if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < CPW; ++c) {
+          for (int c = 0; c < 2; ++c) {
             if (types[c] == 0) continue;
-            const void* tm = types[c] == 1 ? (w == 0 ? (const void*)&p.tm.k_cache
-                                                     : (const void*)&p.tm.v_cache)
-                                           : (w == 0 ? (const void*)&p.tm.k_new
-                                                     : (const void*)&p.tm.v_new);
 #pragma unroll
             for (int db = 0; db < D / 64; ++db)
-              tma_load_3d(sX + db * (C::TN * 128) + (row0 + 16 * c) * 128, tm, db * 64, u.g,
-                          rows[c], bar);
+              tma_load_3d(sX + db * (C::TN * 128) + (row0 + 16 * c) * 128,
+                          types[c] == 1 ? tm_cache : tm_new, db * 64, u.g, rows[c], bar);
             bytes += (D / 64) * kChunkBytes;
           }
         }
-        if (fb_mask != 0) {
-          gather_rows<D, FP8>(p, row0, RPW, fb_mask, cache_rows, w == 0 ? kp : vp, sX);
-          cp_async_commit();
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          __syncwarp();
+        if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
+          const char* mine = nullptr;
+          const int pos = p_row0 + lane;
+          if (pos < u.c) {
+            const int lp = pos / p.page_size;
+            const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
+            if (page >= 0 && page < p.num_pages) {
+              mine = g_cache +
+                     (((size_t)page * p.page_size + (pos - lp * p.page_size)) * p.num_kv_heads +
+                      u.g) * D * kCacheElt;
+            } else {
+              report(p.status, PPA_ERR_BAD_PAGE);
+            }
+          } else if (pos < u.s) {
+            mine = g_new + ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D * 2;
+          }
+          gather_rows<D, FP8>(p, row0, 32, fb_mask, u.c - p_row0, mine, sX);
+          any_fallback = true;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
       }
+      if (any_fallback) {
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     }
     if (!ok) break;
   }
@@ -425,6 +423,8 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         tc_fence_after();
         issue_s(i, s);
       }
+      // every S that reads K(kt) has now been issued (in this or the previous iteration)
+      tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));
       for (int i = 0; i < u.nt && ok; ++i) {
         if (kt < u.lo_i[i] || kt >= u.hi_i[i]) continue;
         if (kt == u.lo_i[i]) {  // O_i must have been read out by the previous epilogue
@@ -452,7 +452,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
           tc_commit(sh.bar(wsbar::O_DONE + 8 * i));
         }
       }
-      tc_commit(sh.bar(wsbar::KV_EMPTY + 8 * s));
+      tc_commit(sh.bar(wsbar::V_EMPTY + 8 * s));
       ++kv_iter;
     }
     tc_commit(sh.bar(wsbar::Q_EMPTY));
@@ -500,12 +500,14 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
         if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
         issue_s(s, sc & 1);
+        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));  // S(kt) is K(kt)'s only reader
       }
       if (kt + 1 < u.hi) {
         const int s2 = (kv_iter + 1) % C::NS;
         if (!sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / C::NS) & 1)) { ok = false; break; }
         tc_fence_after();
         issue_s(s2, (sc + 1) & 1);
+        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
       }
       if (kt == u.lo) {  // O must have been read out by the previous epilogue
         if (!sh.wait(wsbar::O_EMPTY, oe_phase ^ 1)) { ok = false; break; }
@@ -523,7 +525,7 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
         mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
                     kk > 0 ? 1u : acc0);
       tc_commit(sh.bar(wsbar::O_DONE));
-      tc_commit(sh.bar(wsbar::KV_EMPTY + 8 * s));
+      tc_commit(sh.bar(wsbar::V_EMPTY + 8 * s));
       ++kv_iter;
       ++sc;
     }
@@ -734,9 +736,10 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     mbar_init(sh.bar(Q_FULL), 1);  // producer warp 0 lane 0, with the TMA byte count
     mbar_init(sh.bar(Q_EMPTY), 1);
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(sh.bar(K_FULL + 8 * s), 4);  // one arrival (with its TMA bytes) per producer warp
-      mbar_init(sh.bar(V_FULL + 8 * s), 4);
-      mbar_init(sh.bar(KV_EMPTY + 8 * s), 1);
+      mbar_init(sh.bar(K_FULL + 8 * s), 2);  // one arrival (with its TMA bytes) per stream warp
+      mbar_init(sh.bar(V_FULL + 8 * s), 2);
+      mbar_init(sh.bar(K_EMPTY + 8 * s), 1);
+      mbar_init(sh.bar(V_EMPTY + 8 * s), 1);
     }
     mbar_init(sh.bar(FIN), 1);
     *sh.abort = 0;
