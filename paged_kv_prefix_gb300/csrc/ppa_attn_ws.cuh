@@ -392,13 +392,16 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
   const uint64_t dV0 = sdesc_sw128(base + C::KV_OFF + C::KV_BYTES, C::TN * 128, 1024);
   constexpr uint32_t kQStep = C::Q_BYTES >> 4, kStageStep = (2 * C::KV_BYTES) >> 4;
-  uint32_t kv_iter = 0, q_phase = 0;
-  uint32_t pf_phase[2] = {0, 0}, oe_phase[2] = {0, 0};
+  // Per-tile phases as bit i of one word, and the tile intervals read through selects: a
+  // runtime index into a small array would put it in local memory, on this thread's
+  // critical path between MMA batches.
+  uint32_t kv_iter = 0, q_phase = 0, pf_bits = 0, oe_bits = 0;
   bool ok = true;
   for (int k = 0; ok; ++k) {
     const int item = ring_get1(sh, k);
     if (item < 0) break;
     const UnitInfo u = decode_item(p, item);
+    const int lo0 = u.lo_i[0], hi0 = u.hi_i[0], lo1 = u.lo_i[1], hi1 = u.hi_i[1];
     if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
     q_phase ^= 1;
     tc_fence_after();
@@ -418,7 +421,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       const uint32_t ph = (kv_iter / C::NS) & 1;
       // first key tile of a query tile: its S
       for (int i = 0; i < u.nt && ok; ++i) {
-        if (kt != u.lo_i[i]) continue;
+        if (kt != (i ? lo1 : lo0)) continue;
         if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
         issue_s(i, s);
@@ -426,23 +429,24 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       // every S that reads K(kt) has now been issued (in this or the previous iteration)
       tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));
       for (int i = 0; i < u.nt && ok; ++i) {
-        if (kt < u.lo_i[i] || kt >= u.hi_i[i]) continue;
-        if (kt == u.lo_i[i]) {  // O_i must have been read out by the previous epilogue
-          if (!sh.wait(wsbar::O_EMPTY + 8 * i, oe_phase[i] ^ 1)) { ok = false; break; }
-          oe_phase[i] ^= 1;
+        const int lo_i = i ? lo1 : lo0, hi_i = i ? hi1 : hi0;
+        if (kt < lo_i || kt >= hi_i) continue;
+        if (kt == lo_i) {  // O_i must have been read out by the previous epilogue
+          if (!sh.wait(wsbar::O_EMPTY + 8 * i, ((oe_bits >> i) & 1) ^ 1)) { ok = false; break; }
+          oe_bits ^= 1u << i;
         }
-        if (!sh.wait(wsbar::P_FULL + 8 * i, pf_phase[i])) { ok = false; break; }
-        pf_phase[i] ^= 1;
+        if (!sh.wait(wsbar::P_FULL + 8 * i, (pf_bits >> i) & 1)) { ok = false; break; }
+        pf_bits ^= 1u << i;
         if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tP = tmem + C::TM_S + i * C::TN;
         const uint32_t tO = tmem + C::TM_O + i * D;
         const uint64_t b0 = dV0 + s * kStageStep;
-        const uint32_t acc0 = kt > u.lo_i[i] ? 1u : 0u;
+        const uint32_t acc0 = kt > lo_i ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < C::TN / 16; ++kk)
           mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
-        if (kt + 1 < u.hi_i[i]) {
+        if (kt + 1 < hi_i) {
           const int s2 = (kv_iter + 1) % C::NS;
           const uint32_t ph2 = ((kv_iter + 1) / C::NS) & 1;
           if (!sh.wait(wsbar::K_FULL + 8 * s2, ph2)) { ok = false; break; }
