@@ -419,7 +419,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     for (int kt = u.lo; kt < u.hi && ok; ++kt) {
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
-      // first key tile of a query tile: its S
+      // first key tile of a query tile: its S (the one S whose K the issuer waits for)
       for (int i = 0; i < u.nt && ok; ++i) {
         if (kt != (i ? lo1 : lo0)) continue;
         if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
@@ -435,9 +435,12 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
           if (!sh.wait(wsbar::O_EMPTY + 8 * i, ((oe_bits >> i) & 1) ^ 1)) { ok = false; break; }
           oe_bits ^= 1u << i;
         }
+        // P_i(kt) also certifies V(kt) and, unless this is the tile's last key tile,
+        // K(kt+1): the softmax warps waited for both before arriving. The issuer waits on
+        // nothing else here, because each wait leaves the tensor pipe idle (its queue holds
+        // about one MMA).
         if (!sh.wait(wsbar::P_FULL + 8 * i, (pf_bits >> i) & 1)) { ok = false; break; }
         pf_bits ^= 1u << i;
-        if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tP = tmem + C::TM_S + i * C::TN;
         const uint32_t tO = tmem + C::TM_O + i * D;
@@ -447,11 +450,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         for (int kk = 0; kk < C::TN / 16; ++kk)
           mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
         if (kt + 1 < hi_i) {
-          const int s2 = (kv_iter + 1) % C::NS;
-          const uint32_t ph2 = ((kv_iter + 1) / C::NS) & 1;
-          if (!sh.wait(wsbar::K_FULL + 8 * s2, ph2)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(i, s2);
+          issue_s(i, (kv_iter + 1) % C::NS);
         } else {
           tc_commit(sh.bar(wsbar::O_DONE + 8 * i));
         }
@@ -553,10 +552,13 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
   // NQ == 2: one S buffer per tile, S_FULL[i] and O_DONE[i] flip once per use.
   // NQ == 1: S buffers alternate (tile count sc), O_DONE completes once per PV.
   uint32_t sf_phase = 0, od_phase = 0, sc = 0;
+  uint32_t kv_next = 0;  // K/V ring position of the next unit's first key tile
   for (int k = 0;; ++k) {
     const int item = ring_get(sh, k);
     if (item < 0) break;
     const UnitInfo u = decode_item(p, item);
+    const uint32_t kv0 = kv_next;
+    kv_next += u.hi - u.lo;
     if (i >= u.nt) continue;
     const int lo = u.lo_i[i], hi = u.hi_i[i];
     const int tok = r / p.group, hh = r % p.group;
@@ -578,9 +580,20 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     for (int kt = lo; kt < hi; ++kt) {
       const uint32_t buf = C::NQ == 2 ? 0u : (sc & 1);
       const uint32_t tS = tmem + C::TM_S + (i * C::NSB + buf) * C::TN + lane_off;
+      const uint32_t kv = kv0 + (kt - u.lo);  // ring position of key tile kt
+      const uint32_t bar_v = wsbar::V_FULL + 8 * (kv % C::NS), par_v = (kv / C::NS) & 1;
+      const uint32_t bar_k = wsbar::K_FULL + 8 * ((kv + 1) % C::NS), par_k = ((kv + 1) / C::NS) & 1;
+      bool v_ready = true, k_ready = true;
       if constexpr (C::NQ == 2) {
         if (!wait_warp(sh, wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
         sf_phase ^= 1;
+        // V(kt) and K(kt+1) must be resident before P_FULL lets the issuer start PV(kt) and
+        // S(kt+1). Probe both now (non-blocking; the latency overlaps the softmax) and wait
+        // before the arrival only for what was not ready. Probing after S(kt) has landed
+        // is what makes the parity test unambiguous: every earlier fill of these stages that
+        // a tile uses was confirmed before the issuer could issue S(kt).
+        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);
+        k_ready = kt + 1 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
       } else {
         if (!wait_warp(sh, wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
       }
@@ -680,6 +693,10 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         }
       }
       tmem_st_wait();
+      if constexpr (C::NQ == 2) {
+        if (!__all_sync(0xffffffffu, v_ready) && !wait_warp(sh, bar_v, par_v)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, k_ready) && !wait_warp(sh, bar_k, par_k)) { ok = false; break; }
+      }
       tc_fence_before();
       mbar_arrive(sh.bar(wsbar::P_FULL + 8 * i));
     }
