@@ -416,7 +416,38 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       }
       tc_commit(sh.bar(wsbar::S_FULL + 8 * i));
     };
-    for (int kt = u.lo; kt < u.hi && ok; ++kt) {
+    // Steady state: both tiles past their first key tile and with a next one. Straight-line
+    // code whose only taken branch is the back edge: this thread competes for the
+    // instruction cache with the softmax warps' long bodies, and every taken branch into an
+    // evicted line stalls it while the tensor pipe, which queues about one MMA, runs dry.
+    const int steady_lo = u.nt == 2 ? max(lo0, lo1) + 1 : INT_MAX;
+    const int steady_hi = u.nt == 2 ? min(hi0, hi1) - 1 : INT_MIN;
+    auto issue_pv = [&](int i, int stage, uint32_t acc0) {
+      const uint32_t tP = tmem + C::TM_S + i * C::TN;
+      const uint32_t tO = tmem + C::TM_O + i * D;
+      const uint64_t b0 = dV0 + stage * kStageStep;
+#pragma unroll
+      for (int kk = 0; kk < C::TN / 16; ++kk)
+        mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
+    };
+    for (int kt = u.lo; kt < u.hi && ok;) {
+      if (kt >= steady_lo && kt < steady_hi) {
+        for (; kt < steady_hi; ++kt, ++kv_iter) {
+          const int s = kv_iter % C::NS, s1 = (kv_iter + 1) % C::NS;
+          tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));  // both S(kt) were issued last iteration
+          if (!sh.wait(wsbar::P_FULL, pf_bits & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, s, 1u);
+          issue_s(0, s1);
+          if (!sh.wait(wsbar::P_FULL + 8, (pf_bits >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          pf_bits ^= 3u;
+          issue_pv(1, s, 1u);
+          tc_commit(sh.bar(wsbar::V_EMPTY + 8 * s));
+          issue_s(1, s1);
+        }
+        continue;
+      }
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
       // first key tile of a query tile: its S (the one S whose K the issuer waits for)
@@ -442,13 +473,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         if (!sh.wait(wsbar::P_FULL + 8 * i, (pf_bits >> i) & 1)) { ok = false; break; }
         pf_bits ^= 1u << i;
         tc_fence_after();
-        const uint32_t tP = tmem + C::TM_S + i * C::TN;
-        const uint32_t tO = tmem + C::TM_O + i * D;
-        const uint64_t b0 = dV0 + s * kStageStep;
-        const uint32_t acc0 = kt > lo_i ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < C::TN / 16; ++kk)
-          mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
+        issue_pv(i, s, kt > lo_i ? 1u : 0u);
         if (kt + 1 < hi_i) {
           issue_s(i, (kv_iter + 1) % C::NS);
         } else {
@@ -457,6 +482,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       }
       tc_commit(sh.bar(wsbar::V_EMPTY + 8 * s));
       ++kv_iter;
+      ++kt;
     }
     tc_commit(sh.bar(wsbar::Q_EMPTY));
   }
