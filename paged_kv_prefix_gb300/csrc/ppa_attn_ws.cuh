@@ -522,7 +522,33 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
     if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
     q_phase ^= 1;
     tc_fence_after();
-    for (int kt = u.lo; kt < u.hi; ++kt) {
+    auto issue_pv = [&](int stage, uint32_t buf, uint32_t acc0) {
+      const uint32_t tP = tmem + C::TM_S + buf * C::TN;
+      const uint64_t b0 = dV0 + stage * kStageStep;
+#pragma unroll
+      for (int kk = 0; kk < C::TN / 16; ++kk)
+        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
+                    kk > 0 ? 1u : acc0);
+      tc_commit(sh.bar(wsbar::O_DONE));
+      tc_commit(sh.bar(wsbar::V_EMPTY + 8 * stage));
+    };
+    for (int kt = u.lo; kt < u.hi && ok;) {
+      // Steady state (not the first key tile, a next one exists): straight-line code, two
+      // waits per key tile. P(kt) also certifies V(kt): the softmax waited for it.
+      if (kt > u.lo && kt + 1 < u.hi) {
+        for (; kt + 1 < u.hi; ++kt, ++kv_iter, ++sc) {
+          const int s = kv_iter % C::NS, s2 = (kv_iter + 1) % C::NS;
+          if (!sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / C::NS) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(s2, (sc + 1) & 1);
+          tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
+          if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }
+          pf_phase ^= 1;
+          tc_fence_after();
+          issue_pv(s, sc & 1, 1u);
+        }
+        continue;
+      }
       const int s = kv_iter % C::NS;
       const uint32_t ph = (kv_iter / C::NS) & 1;
       if (kt == u.lo) {
@@ -542,21 +568,13 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
         if (!sh.wait(wsbar::O_EMPTY, oe_phase ^ 1)) { ok = false; break; }
         oe_phase ^= 1;
       }
-      if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }
+      if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }  // certifies V(kt)
       pf_phase ^= 1;
-      if (!sh.wait(wsbar::V_FULL + 8 * s, ph)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tP = tmem + C::TM_S + (sc & 1) * C::TN;
-      const uint64_t b0 = dV0 + s * kStageStep;
-      const uint32_t acc0 = kt > u.lo ? 1u : 0u;
-#pragma unroll
-      for (int kk = 0; kk < C::TN / 16; ++kk)
-        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
-                    kk > 0 ? 1u : acc0);
-      tc_commit(sh.bar(wsbar::O_DONE));
-      tc_commit(sh.bar(wsbar::V_EMPTY + 8 * s));
+      issue_pv(s, sc & 1, kt > u.lo ? 1u : 0u);
       ++kv_iter;
       ++sc;
+      ++kt;
     }
     tc_commit(sh.bar(wsbar::Q_EMPTY));
   }
@@ -622,6 +640,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         k_ready = kt + 1 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
       } else {
         if (!wait_warp(sh, wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
+        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);  // same reasoning, V(kt) only
       }
       ++sc;
       tc_fence_after();
@@ -719,8 +738,8 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         }
       }
       tmem_st_wait();
+      if (!__all_sync(0xffffffffu, v_ready) && !wait_warp(sh, bar_v, par_v)) { ok = false; break; }
       if constexpr (C::NQ == 2) {
-        if (!__all_sync(0xffffffffu, v_ready) && !wait_warp(sh, bar_v, par_v)) { ok = false; break; }
         if (!__all_sync(0xffffffffu, k_ready) && !wait_warp(sh, bar_k, par_k)) { ok = false; break; }
       }
       tc_fence_before();
