@@ -50,13 +50,20 @@ struct WsCfg {
   static constexpr int NQ = D <= 128 ? 2 : 1;  // query tiles per unit
   static constexpr int TN = D <= 128 ? 128 : 64;  // keys per key tile
   static constexpr int NSB = NQ == 2 ? 1 : 2;  // S buffers per query tile
-  static constexpr int NS = D == 64 ? 4 : 2;  // K/V pipeline stages
+  // K and V rings: D = 256 keeps a third K stage so that K(kt+2) is resident by the time the
+  // softmax of tile kt certifies it (the single-tile issuer waits on P alone).
+  static constexpr int NSK = D == 64 ? 4 : (D == 256 ? 3 : 2);  // K stages
+  static constexpr int NSV = D == 64 ? 4 : 2;                    // V stages
   static constexpr int CPR = D / 8;       // 16-byte chunks per bf16 row
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int KV_BYTES = TN * D * 2;
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;  // stage s: K at +2s*KV, V at +(2s+1)*KV
-  static constexpr int BAR_OFF = KV_OFF + NS * 2 * KV_BYTES;
+  // K stage s at KV_OFF + s*STAGE_STRIDE, V stage s at V_OFF + s*STAGE_STRIDE: interleaved
+  // (K, V, K, V, ...) when both rings have the same depth, two separate rings otherwise.
+  static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;
+  static constexpr int STAGE_STRIDE = NSK == NSV ? 2 * KV_BYTES : KV_BYTES;
+  static constexpr int V_OFF = NSK == NSV ? KV_OFF + KV_BYTES : KV_OFF + NSK * KV_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + (NSK + NSV) * KV_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int TM_O = 0;       // O_i at column TM_O + i*D
@@ -296,10 +303,11 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
     // ---- this warp's rows of the K (or V) tiles of the union interval ----
     bool ok = true;
     for (int kt = u.lo; kt < u.hi; ++kt, ++kv_iter) {
-      const int s = kv_iter % C::NS;
-      const uint32_t ph = (kv_iter / C::NS) & 1;
+      const int ns = C::NSK == C::NSV ? C::NSK : (w == 0 ? C::NSK : C::NSV);
+      const int s = kv_iter % ns;
+      const uint32_t ph = (kv_iter / ns) & 1;
       if (!wait_warp(sh, empty_bar + 8 * s, ph ^ 1)) { ok = false; break; }
-      const uint32_t sX = base + C::KV_OFF + (2 * s + w) * C::KV_BYTES;
+      const uint32_t sX = base + (w == 0 ? C::KV_OFF : C::V_OFF) + s * C::STAGE_STRIDE;
       const uint32_t bar = sh.bar(full_bar + 8 * s);
       uint32_t bytes = 0;
       bool any_fallback = false;
@@ -390,8 +398,10 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   // 14-bit start-address field, which cannot carry because shared addresses stay below 256 KB.
   const uint64_t dQ0 = sdesc_sw128(base + C::Q_OFF, 16, 1024);
   const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
-  const uint64_t dV0 = sdesc_sw128(base + C::KV_OFF + C::KV_BYTES, C::TN * 128, 1024);
-  constexpr uint32_t kQStep = C::Q_BYTES >> 4, kStageStep = (2 * C::KV_BYTES) >> 4;
+  const uint64_t dV0 = sdesc_sw128(base + C::V_OFF, C::TN * 128, 1024);
+  constexpr uint32_t kQStep = C::Q_BYTES >> 4, kStageStep = C::STAGE_STRIDE >> 4;
+  static_assert(C::NSK == C::NSV, "two-tile units use one ring position for K and V");
+  constexpr int NS = C::NSK;
   // Per-tile phases as bit i of one word, and the tile intervals read through selects: a
   // runtime index into a small array would put it in local memory, on this thread's
   // critical path between MMA batches.
@@ -407,7 +417,10 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     tc_fence_after();
     auto issue_s = [&](int i, int stage) {
       const uint32_t tS = tmem + C::TM_S + i * C::TN;
-      const uint64_t a0 = dQ0 + i * kQStep, b0 = dK0 + stage * kStageStep;
+      uint64_t a0 = dQ0 + i * kQStep, b0 = dK0 + stage * kStageStep;
+      // Opaque to the compiler: otherwise it hoists every per-MMA descriptor of the
+      // unrolled batches out of the loop into registers and spills them to local memory.
+      asm volatile("" : "+l"(a0), "+l"(b0));
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off_a = ((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4;
@@ -425,7 +438,8 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     auto issue_pv = [&](int i, int stage, uint32_t acc0) {
       const uint32_t tP = tmem + C::TM_S + i * C::TN;
       const uint32_t tO = tmem + C::TM_O + i * D;
-      const uint64_t b0 = dV0 + stage * kStageStep;
+      uint64_t b0 = dV0 + stage * kStageStep;
+      asm volatile("" : "+l"(b0));
 #pragma unroll
       for (int kk = 0; kk < C::TN / 16; ++kk)
         mma_bf16_ts(tO, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO, kk > 0 ? 1u : acc0);
@@ -433,7 +447,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     for (int kt = u.lo; kt < u.hi && ok;) {
       if (kt >= steady_lo && kt < steady_hi) {
         for (; kt < steady_hi; ++kt, ++kv_iter) {
-          const int s = kv_iter % C::NS, s1 = (kv_iter + 1) % C::NS;
+          const int s = kv_iter % NS, s1 = (kv_iter + 1) % NS;
           tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));  // both S(kt) were issued last iteration
           if (!sh.wait(wsbar::P_FULL, pf_bits & 1)) { ok = false; break; }
           tc_fence_after();
@@ -448,8 +462,8 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         }
         continue;
       }
-      const int s = kv_iter % C::NS;
-      const uint32_t ph = (kv_iter / C::NS) & 1;
+      const int s = kv_iter % NS;
+      const uint32_t ph = (kv_iter / NS) & 1;
       // first key tile of a query tile: its S (the one S whose K the issuer waits for)
       for (int i = 0; i < u.nt && ok; ++i) {
         if (kt != (i ? lo1 : lo0)) continue;
@@ -475,7 +489,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
         tc_fence_after();
         issue_pv(i, s, kt > lo_i ? 1u : 0u);
         if (kt + 1 < hi_i) {
-          issue_s(i, (kv_iter + 1) % C::NS);
+          issue_s(i, (kv_iter + 1) % NS);
         } else {
           tc_commit(sh.bar(wsbar::O_DONE + 8 * i));
         }
@@ -501,16 +515,18 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
   uint32_t kv_iter = 0, q_phase = 0, pf_phase = 0, oe_phase = 0, sc = 0;
   const uint64_t dQ = sdesc_sw128(base + C::Q_OFF, 16, 1024);
   const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
-  const uint64_t dV0 = sdesc_sw128(base + C::KV_OFF + C::KV_BYTES, C::TN * 128, 1024);
-  constexpr uint32_t kStageStep = (2 * C::KV_BYTES) >> 4;
+  const uint64_t dV0 = sdesc_sw128(base + C::V_OFF, C::TN * 128, 1024);
+  constexpr uint32_t kStageStep = C::STAGE_STRIDE >> 4;
+  constexpr int NSK = C::NSK, NSV = C::NSV;
   auto issue_s = [&](int stage, uint32_t buf) {
     const uint32_t tS = tmem + C::TM_S + buf * C::TN;
-    const uint64_t b0 = dK0 + stage * kStageStep;
+    uint64_t a0 = dQ, b0 = dK0 + stage * kStageStep;
+    asm volatile("" : "+l"(a0), "+l"(b0));  // keep per-MMA descriptors out of registers
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off_a = ((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4;
       const uint32_t off_b = ((kk >> 2) * (C::TN * 128) + (kk & 3) * 32) >> 4;
-      mma_bf16_ss(tS, dQ + off_a, b0 + off_b, kIdescS, kk > 0 ? 1u : 0u);
+      mma_bf16_ss(tS, a0 + off_a, b0 + off_b, kIdescS, kk > 0 ? 1u : 0u);
     }
     tc_commit(sh.bar(wsbar::S_FULL + 8 * buf));
   };
@@ -524,7 +540,8 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
     tc_fence_after();
     auto issue_pv = [&](int stage, uint32_t buf, uint32_t acc0) {
       const uint32_t tP = tmem + C::TM_S + buf * C::TN;
-      const uint64_t b0 = dV0 + stage * kStageStep;
+      uint64_t b0 = dV0 + stage * kStageStep;
+      asm volatile("" : "+l"(b0));
 #pragma unroll
       for (int kk = 0; kk < C::TN / 16; ++kk)
         mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
@@ -535,31 +552,31 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
     for (int kt = u.lo; kt < u.hi && ok;) {
       // Steady state (not the first key tile, a next one exists): straight-line code, two
       // waits per key tile. P(kt) also certifies V(kt): the softmax waited for it.
+      // Steady state (kt > lo, a next tile exists): S(kt+1) needs K(kt+1), which P(kt-1)
+      // certified (kt+1 >= lo+2), so the only wait per key tile is P(kt).
       if (kt > u.lo && kt + 1 < u.hi) {
         for (; kt + 1 < u.hi; ++kt, ++kv_iter, ++sc) {
-          const int s = kv_iter % C::NS, s2 = (kv_iter + 1) % C::NS;
-          if (!sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / C::NS) & 1)) { ok = false; break; }
-          tc_fence_after();
+          const int sv = kv_iter % NSV, s2 = (kv_iter + 1) % NSK;
           issue_s(s2, (sc + 1) & 1);
           tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
           if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }
           pf_phase ^= 1;
           tc_fence_after();
-          issue_pv(s, sc & 1, 1u);
+          issue_pv(sv, sc & 1, 1u);
         }
         continue;
       }
-      const int s = kv_iter % C::NS;
-      const uint32_t ph = (kv_iter / C::NS) & 1;
-      if (kt == u.lo) {
-        if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
+      const int sk = kv_iter % NSK, sv = kv_iter % NSV;
+      if (kt == u.lo) {  // the unit's first two S: no P certifies their K yet
+        if (!sh.wait(wsbar::K_FULL + 8 * sk, (kv_iter / NSK) & 1)) { ok = false; break; }
         tc_fence_after();
-        issue_s(s, sc & 1);
-        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));  // S(kt) is K(kt)'s only reader
+        issue_s(sk, sc & 1);
+        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * sk));  // S(kt) is K(kt)'s only reader
       }
       if (kt + 1 < u.hi) {
-        const int s2 = (kv_iter + 1) % C::NS;
-        if (!sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / C::NS) & 1)) { ok = false; break; }
+        const int s2 = (kv_iter + 1) % NSK;
+        if (kt == u.lo &&
+            !sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / NSK) & 1)) { ok = false; break; }
         tc_fence_after();
         issue_s(s2, (sc + 1) & 1);
         tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
@@ -571,7 +588,7 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
       if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }  // certifies V(kt)
       pf_phase ^= 1;
       tc_fence_after();
-      issue_pv(s, sc & 1, kt > u.lo ? 1u : 0u);
+      issue_pv(sv, sc & 1, kt > u.lo ? 1u : 0u);
       ++kv_iter;
       ++sc;
       ++kt;
@@ -625,8 +642,12 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       const uint32_t buf = C::NQ == 2 ? 0u : (sc & 1);
       const uint32_t tS = tmem + C::TM_S + (i * C::NSB + buf) * C::TN + lane_off;
       const uint32_t kv = kv0 + (kt - u.lo);  // ring position of key tile kt
-      const uint32_t bar_v = wsbar::V_FULL + 8 * (kv % C::NS), par_v = (kv / C::NS) & 1;
-      const uint32_t bar_k = wsbar::K_FULL + 8 * ((kv + 1) % C::NS), par_k = ((kv + 1) / C::NS) & 1;
+      // K certified with P(kt): K(kt+1) for two-tile units (S(kt+1) follows PV(kt)), K(kt+2)
+      // for one-tile units (S(kt+2) is issued after P(kt) is seen, before PV(kt+1)).
+      constexpr uint32_t kAhead = C::NQ == 2 ? 1 : 2;
+      const uint32_t bar_v = wsbar::V_FULL + 8 * (kv % C::NSV), par_v = (kv / C::NSV) & 1;
+      const uint32_t bar_k = wsbar::K_FULL + 8 * ((kv + kAhead) % C::NSK);
+      const uint32_t par_k = ((kv + kAhead) / C::NSK) & 1;
       bool v_ready = true, k_ready = true;
       if constexpr (C::NQ == 2) {
         if (!wait_warp(sh, wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
@@ -640,7 +661,10 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         k_ready = kt + 1 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
       } else {
         if (!wait_warp(sh, wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
-        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);  // same reasoning, V(kt) only
+        // Same reasoning. The previous fill of K(kt+2)'s stage, K(kt-1), was confirmed
+        // before S(kt-1), hence before S(kt).
+        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);
+        k_ready = kt + 2 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
       }
       ++sc;
       tc_fence_after();
@@ -739,9 +763,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       }
       tmem_st_wait();
       if (!__all_sync(0xffffffffu, v_ready) && !wait_warp(sh, bar_v, par_v)) { ok = false; break; }
-      if constexpr (C::NQ == 2) {
-        if (!__all_sync(0xffffffffu, k_ready) && !wait_warp(sh, bar_k, par_k)) { ok = false; break; }
-      }
+      if (!__all_sync(0xffffffffu, k_ready) && !wait_warp(sh, bar_k, par_k)) { ok = false; break; }
       tc_fence_before();
       mbar_arrive(sh.bar(wsbar::P_FULL + 8 * i));
     }
@@ -801,10 +823,12 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     }
     mbar_init(sh.bar(Q_FULL), 1);  // producer warp 0 lane 0, with the TMA byte count
     mbar_init(sh.bar(Q_EMPTY), 1);
-    for (int s = 0; s < C::NS; ++s) {
+    for (int s = 0; s < C::NSK; ++s) {
       mbar_init(sh.bar(K_FULL + 8 * s), 2);  // one arrival (with its TMA bytes) per stream warp
-      mbar_init(sh.bar(V_FULL + 8 * s), 2);
       mbar_init(sh.bar(K_EMPTY + 8 * s), 1);
+    }
+    for (int s = 0; s < C::NSV; ++s) {
+      mbar_init(sh.bar(V_FULL + 8 * s), 2);
       mbar_init(sh.bar(V_EMPTY + 8 * s), 1);
     }
     mbar_init(sh.bar(FIN), 1);
