@@ -473,6 +473,9 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       }
       // every S that reads K(kt) has now been issued (in this or the previous iteration)
       tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));
+      // At the unit's last key tile every S has been issued: Q is free once they complete,
+      // so the next unit's Q loads while this unit's last PVs and softmax run.
+      if (kt == u.hi - 1) tc_commit(sh.bar(wsbar::Q_EMPTY));
       for (int i = 0; i < u.nt && ok; ++i) {
         const int lo_i = i ? lo1 : lo0, hi_i = i ? hi1 : hi0;
         if (kt < lo_i || kt >= hi_i) continue;
@@ -498,7 +501,6 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       ++kv_iter;
       ++kt;
     }
-    tc_commit(sh.bar(wsbar::Q_EMPTY));
   }
 }
 
@@ -573,6 +575,7 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
         issue_s(sk, sc & 1);
         tc_commit(sh.bar(wsbar::K_EMPTY + 8 * sk));  // S(kt) is K(kt)'s only reader
       }
+      if (kt == u.hi - 1) tc_commit(sh.bar(wsbar::Q_EMPTY));  // every S issued: free Q early
       if (kt + 1 < u.hi) {
         const int s2 = (kv_iter + 1) % NSK;
         if (kt == u.lo &&
@@ -593,7 +596,6 @@ __device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t 
       ++sc;
       ++kt;
     }
-    tc_commit(sh.bar(wsbar::Q_EMPTY));
   }
 }
 
