@@ -222,11 +222,15 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   bool maps_ok =
       encode_rows(&a.tm.q, q, D, dims->num_q_heads, dims->total_q, G, tq) &&
       encode_rows(&a.tm.k_new, k_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
-      encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16);
+      encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
+      encode_rows(&a.tm.k_new32, k_new, D, dims->num_kv_heads, dims->total_q, 1, 32) &&
+      encode_rows(&a.tm.v_new32, v_new, D, dims->num_kv_heads, dims->total_q, 1, 32);
   if (maps_ok && !fp8) {
     const long long cache_rows = (long long)dims->num_pages * dims->page_size;
     maps_ok = encode_rows(&a.tm.k_cache, k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
-              encode_rows(&a.tm.v_cache, v_cache, D, dims->num_kv_heads, cache_rows, 1, 16);
+              encode_rows(&a.tm.v_cache, v_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
+              encode_rows(&a.tm.k_cache32, k_cache, D, dims->num_kv_heads, cache_rows, 1, 32) &&
+              encode_rows(&a.tm.v_cache32, v_cache, D, dims->num_kv_heads, cache_rows, 1, 32);
   }
   if (!maps_ok) return PPA_ERR_CUDA;
   const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);

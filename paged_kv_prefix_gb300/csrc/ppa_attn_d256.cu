@@ -1,12 +1,12 @@
-// Attention kernel instances for head_dim 256 (bf16 and fp8 e4m3 KV caches): the
-// warp-specialised kernel with one query tile per unit and a double-buffered S.
-#include "ppa_attn_ws.cuh"
+// Attention kernel instances for head_dim 256 (bf16 and fp8 e4m3 KV caches): the CTA-pair
+// kernel, M = 256 tcgen05 MMAs over two SMs with 128-key tiles.
+#include "ppa_attn_pair.cuh"
 
 namespace ppa {
 
 cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream) {
-  return fp8 ? launch_attn_ws<256, true>(p, max_items, stream)
-             : launch_attn_ws<256, false>(p, max_items, stream);
+  return fp8 ? launch_attn_pair<256, true>(p, max_items, stream)
+             : launch_attn_pair<256, false>(p, max_items, stream);
 }
 
 }  // namespace ppa

@@ -3,9 +3,10 @@
 // One persistent CTA per SM, 16 warps:
 //   warps 0-3   softmax for query tile A (one thread per row)     \ 184 registers each
 //   warps 4-7   softmax for query tile B                          /
-//   warps 8-11  producers: TMA / cp.async paged K/V gather and Q   \ 72 registers each
+//   warps 8-11  producers: TMA / cp.async paged K/V gather          \ 72 registers each
 //   warp  12    MMA issue (lane 0)                                  |
-//   warps 13-15 idle                                               /
+//   warp  13    Q loads and the item ring                           |
+//   warps 14-15 idle                                               /
 // A unit of work is two consecutive 128-row query tiles (tq tokens x G heads each, token
 // major) of one sequence and one KV head; both tiles consume one stream of K/V tiles, so each
 // tile is gathered once for 256 query rows. Per key tile kt the MMA warp issues, for each
@@ -82,7 +83,7 @@ constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL 
               V_FULL = 80, K_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
               O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224,
               V_EMPTY = 240;
-constexpr int kRingConsumers = 13;  // warps 0..12 each release a ring slot once
+constexpr int kRingConsumers = 14;  // warps 0..13 each release a ring slot once
 }  // namespace wsbar
 
 struct WsShared {
@@ -188,14 +189,15 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 // ---------------------------------------------------------------------------------------
 // Producer role (warps 8-11).
 //
-// Q: producer warp 0 loads each query tile with one TMA box per 64-column block; the box
-// {64 columns, G heads, tq tokens} lands as token-major rows, exactly the MMA's A operand.
+// Q (the Q loader, warp 13): one TMA box per 64-column block; the box {64 columns, G heads,
+// tq tokens} lands as token-major rows, exactly the MMA's A operand.
 // K/V: warps 0-1 stream K and warps 2-3 stream V, each owning half of every key tile, with
 // separate empty barriers: a K slot frees as soon as the S MMAs that read it are issued, a V
 // slot after its PV, so K runs up to two tiles ahead of V. A chunk of 16 keys that are cached
 // context in one page, or are all new tokens, is one TMA box per 64-column block from the
 // cache or the k_new/v_new tensor (rows past the sequence read the next sequence's tokens or
-// the zero fill beyond the tensor: finite values that the mask removes). Any other chunk (it
+// the zero fill beyond the tensor: finite values that the mask removes); two such chunks that
+// are contiguous in their source are one 32-row box. Any other chunk (it
 // straddles the context end or a page boundary; the page id is out of range; the cache is fp8
 // and must be widened) is gathered row by row with cp.async, as the PR #54194 report describes
 // for per-token offsets. Each warp then arrives once on k_full / v_full with the byte count of
@@ -265,40 +267,27 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const int pw = (threadIdx.x >> 5) - 8;  // 0..3
   const int w = pw >> 1;                  // 0: the K stream, 1: the V stream
   const int half = pw & 1;
-  const bool leader = pw == 0 && lane == 0;
   const void* tm_new = w == 0 ? (const void*)&p.tm.k_new : (const void*)&p.tm.v_new;
   const void* tm_cache = w == 0 ? (const void*)&p.tm.k_cache : (const void*)&p.tm.v_cache;
+  const void* tm_new32 = w == 0 ? (const void*)&p.tm.k_new32 : (const void*)&p.tm.v_new32;
+  const void* tm_cache32 = w == 0 ? (const void*)&p.tm.k_cache32 : (const void*)&p.tm.v_cache32;
   const char* g_cache = static_cast<const char*>(w == 0 ? p.k_cache : p.v_cache);
   const char* g_new = static_cast<const char*>(w == 0 ? p.k_new : p.v_new);
   if (lane == 0) {
     tma_prefetch_desc(tm_new);
-    if constexpr (!FP8) tma_prefetch_desc(tm_cache);
-    if (pw == 0) tma_prefetch_desc(&p.tm.q);
+    tma_prefetch_desc(tm_new32);
+    if constexpr (!FP8) {
+      tma_prefetch_desc(tm_cache);
+      tma_prefetch_desc(tm_cache32);
+    }
   }
   const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
   const int full_bar = w == 0 ? wsbar::K_FULL : wsbar::V_FULL;
-  uint32_t kv_iter = 0, q_phase = 0;
+  uint32_t kv_iter = 0;
   for (int k = 0;; ++k) {
-    if (leader) ring_put(sh, p, k, n_items);
     const int item = ring_get(sh, k);
     if (item < 0) break;
     const UnitInfo u = decode_item(p, item);
-
-    // ---- Q tiles ----
-    if (pw == 0) {
-      if (!wait_warp(sh, wsbar::Q_EMPTY, q_phase ^ 1)) break;
-      q_phase ^= 1;
-      if (lane == 0) {
-        const uint32_t box_bytes = static_cast<uint32_t>(p.group * p.tq * 128);
-        mbar_arrive_expect_tx(sh.bar(wsbar::Q_FULL), u.nt * (D / 64) * box_bytes);
-        for (int i = 0; i < u.nt; ++i) {
-#pragma unroll
-          for (int db = 0; db < D / 64; ++db)
-            tma_load_3d(base + C::Q_OFF + i * C::Q_BYTES + db * (C::M * 128), &p.tm.q, db * 64,
-                        u.g * p.group, u.q_start + (u.t0 + i) * p.tq, sh.bar(wsbar::Q_FULL));
-        }
-      }
-    }
 
     // ---- this warp's rows of the K (or V) tiles of the union interval ----
     bool ok = true;
@@ -306,6 +295,25 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       const int ns = C::NSK == C::NSV ? C::NSK : (w == 0 ? C::NSK : C::NSV);
       const int s = kv_iter % ns;
       const uint32_t ph = (kv_iter / ns) & 1;
+      // Classify this warp's 16-row chunks before waiting for the stage, so that the
+      // block-table loads overlap the wait. Lane c < RPW/16 takes chunk c.
+      int ctype = 0, crow = 0;  // 1 = cache box, 2 = new-token box, 0 = row gather
+      if (lane * 16 < RPW) {
+        const int p0 = kt * C::TN + half * RPW + 16 * lane;
+        if (p0 >= u.c) {
+          ctype = 2;
+          crow = u.q_start + p0 - u.c;
+        } else if (!FP8 && p0 + 15 < u.c) {
+          const int lp = p0 / p.page_size;
+          if ((p0 + 15) / p.page_size == lp) {
+            const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
+            if (page >= 0 && page < p.num_pages) {
+              ctype = 1;
+              crow = page * p.page_size + (p0 - lp * p.page_size);
+            }
+          }
+        }
+      }
       if (!wait_warp(sh, empty_bar + 8 * s, ph ^ 1)) { ok = false; break; }
       const uint32_t sX = base + (w == 0 ? C::KV_OFF : C::V_OFF) + s * C::STAGE_STRIDE;
       const uint32_t bar = sh.bar(full_bar + 8 * s);
@@ -315,33 +323,24 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       for (int sub = 0; sub < NSUB; ++sub) {
         const int row0 = half * RPW + 32 * sub;
         const int p_row0 = kt * C::TN + row0;  // key position of this block's first row
-        // chunk classification (lane c < 2): 1 = cache box, 2 = new-token box, 0 = row gather
-        int ctype = 0, crow = 0;
-        if (lane < 2) {
-          const int p0 = p_row0 + 16 * lane;
-          if (p0 >= u.c) {
-            ctype = 2;
-            crow = u.q_start + p0 - u.c;
-          } else if (!FP8 && p0 + 15 < u.c) {
-            const int lp = p0 / p.page_size;
-            if ((p0 + 15) / p.page_size == lp) {
-              const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
-              if (page >= 0 && page < p.num_pages) {
-                ctype = 1;
-                crow = page * p.page_size + (p0 - lp * p.page_size);
-              }
-            }
-          }
-        }
         int types[2], rows[2];
         uint32_t fb_mask = 0;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          types[c] = __shfl_sync(0xffffffffu, ctype, c);
-          rows[c] = __shfl_sync(0xffffffffu, crow, c);
+          types[c] = __shfl_sync(0xffffffffu, ctype, 2 * sub + c);
+          rows[c] = __shfl_sync(0xffffffffu, crow, 2 * sub + c);
           if (types[c] == 0) fb_mask |= 0xFFFFu << (16 * c);
         }
-        if (lane == 0) {
+        // both chunks from one contiguous source run: one 32-row box per column block
+        const bool one_run = types[0] != 0 && types[0] == types[1] && rows[1] == rows[0] + 16;
+        if (lane == 0 && one_run) {
+          const void* tm32 = types[0] == 1 ? tm_cache32 : tm_new32;
+#pragma unroll
+          for (int db = 0; db < D / 64; ++db)
+            tma_load_3d(sX + db * (C::TN * 128) + row0 * 128, tm32, db * 64, u.g, rows[0], bar);
+          bytes += (D / 64) * 2 * kChunkBytes;
+        }
+        if (lane == 0 && !one_run) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             if (types[c] == 0) continue;
@@ -383,6 +382,34 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
     if (!ok) break;
   }
   cp_async_wait<0>();
+}
+
+// Q loader (warp 13): runs the item ring and loads each unit's query tiles, so that the K
+// and V streams never wait for Q_EMPTY at a unit boundary and prefetch across units.
+template <int D>
+__device__ void ws_qloader(const AttnParams& p, const WsShared& sh, uint32_t base, int n_items) {
+  using C = WsCfg<D>;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) tma_prefetch_desc(&p.tm.q);
+  uint32_t q_phase = 0;
+  for (int k = 0;; ++k) {
+    if (lane == 0) ring_put(sh, p, k, n_items);
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
+    if (!wait_warp(sh, wsbar::Q_EMPTY, q_phase ^ 1)) break;
+    q_phase ^= 1;
+    if (lane == 0) {
+      const uint32_t box_bytes = static_cast<uint32_t>(p.group * p.tq * 128);
+      mbar_arrive_expect_tx(sh.bar(wsbar::Q_FULL), u.nt * (D / 64) * box_bytes);
+      for (int i = 0; i < u.nt; ++i) {
+#pragma unroll
+        for (int db = 0; db < D / 64; ++db)
+          tma_load_3d(base + C::Q_OFF + i * C::Q_BYTES + db * (C::M * 128), &p.tm.q, db * 64,
+                      u.g * p.group, u.q_start + (u.t0 + i) * p.tq, sh.bar(wsbar::Q_FULL));
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -823,7 +850,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
       mbar_init(sh.bar(O_DONE + 8 * s), 1);
       mbar_init(sh.bar(O_EMPTY + 8 * s), 128);
     }
-    mbar_init(sh.bar(Q_FULL), 1);  // producer warp 0 lane 0, with the TMA byte count
+    mbar_init(sh.bar(Q_FULL), 1);  // the Q loader, with the TMA byte count
     mbar_init(sh.bar(Q_EMPTY), 1);
     for (int s = 0; s < C::NSK; ++s) {
       mbar_init(sh.bar(K_FULL + 8 * s), 2);  // one arrival (with its TMA bytes) per stream warp
@@ -854,6 +881,8 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp < 12) {
       ws_producer<D, FP8>(p, sh, base, n_items);
+    } else if (warp == 13) {
+      ws_qloader<D>(p, sh, base, n_items);
     } else if (warp == 12) {
       if constexpr (C::NQ == 2) {
         ws_mma<D>(p, sh, base, tmem);

@@ -114,6 +114,6 @@ __device__ __forceinline__ void tile_interval(int q_lo, int q_hi, int s, const M
 
 // Tile shape for a head group of G query heads: tq tokens x G heads <= 128 rows.
 __host__ __device__ constexpr int tokens_per_qtile(int group) { return kRowsPerTile / group; }
-__host__ __device__ constexpr int keys_per_tile(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+__host__ __device__ constexpr int keys_per_tile(int) { return 128; }
 
 }  // namespace ppa

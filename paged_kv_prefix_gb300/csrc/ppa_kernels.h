@@ -37,8 +37,11 @@ struct Stage1Params {
 //   k_new, v_new  [total_q][Hkv][D] bf16, box {64, 1, 16}: 16 keys of one KV head
 //   k_cache, v_cache [num_pages * P][Hkv][D] bf16, box {64, 1, 16} (unused for fp8 caches)
 // All use the 128-byte swizzle, matching the operand layout of the MMAs.
+// Boxes of {64 columns, 1 head, 16 rows}, and the same tensors with 32-row boxes for key
+// blocks that are contiguous in their source (one page, or all new tokens).
 struct TmaMaps {
   CUtensorMap q, k_new, v_new, k_cache, v_cache;
+  CUtensorMap k_new32, v_new32, k_cache32, v_cache32;
 };
 
 struct AttnParams {
@@ -68,7 +71,9 @@ cudaError_t launch_tile_bounds(const Stage1Params& p, cudaStream_t stream);
 
 // Query tiles per unit of work for a head dimension: two 128-row tiles share each K/V tile
 // when both fit in TMEM and shared memory (D <= 128), otherwise one.
-__host__ __device__ constexpr int tiles_per_unit(int head_dim) { return head_dim <= 128 ? 2 : 1; }
+// Two consecutive query tiles per unit: one CTA's ping-pong pair (head_dim <= 128) or the two
+// CTAs of a pair, one tile each (head_dim 256).
+__host__ __device__ constexpr int tiles_per_unit(int) { return 2; }
 cudaError_t launch_debug_mask(const MaskParams& mp, int seq, const int32_t* cu, const int32_t* ctx,
                               uint32_t* bitmap, int max_rows, int words_per_row,
                               cudaStream_t stream);

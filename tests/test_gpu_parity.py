@@ -70,6 +70,17 @@ def test_fp8_kv_scaled():
     parity(wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=9, scale=1 / 16, num_seqs=4))
 
 
+@pytest.mark.parametrize("page", [16, 37])
+@pytest.mark.parametrize("windowed", [False, True])
+def test_fp8_kv_head_dim_256(page, windowed):
+    """fp8 cache at head_dim 256: each CTA of the pair widens its half of every K and V row."""
+    rng = np.random.default_rng(page + 2 * windowed)
+    ctx = [0, 45, int(rng.integers(200, 400)), 130]
+    qlen = [17, 1, int(rng.integers(150, 300)), 64]
+    parity(wl.build_case("fp8_d256", ctx, qlen, 8, 4, 256, page, causal=True,
+                         window_left=100 if windowed else 0, kv_dtype="fp8_e4m3", seed=page))
+
+
 def test_page_permutation_is_bitwise_invariant():
     a = wl.build_case("perm", [300, 1000], [200, 333], 8, 2, 128, 544, causal=True, seed=10,
                       value_rng_seed=77)

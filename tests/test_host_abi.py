@@ -46,7 +46,7 @@ def test_tiles_and_workspace():
     d = _dims()
     assert binding.ppa_query_tiles(d) == (64, 128)  # G = 2 -> 64 tokens x 2 heads
     assert binding.ppa_workspace_bytes(d) > 0
-    assert binding.ppa_query_tiles(_dims(num_q_heads=32, num_kv_heads=4, head_dim=256)) == (16, 64)
+    assert binding.ppa_query_tiles(_dims(num_q_heads=32, num_kv_heads=4, head_dim=256)) == (16, 128)
     assert binding.ppa_query_tiles(_dims(num_q_heads=6, num_kv_heads=2)) == (42, 128)
     assert binding.ppa_workspace_bytes(_dims(head_dim=96)) == 0
     assert binding.ppa_query_tiles(_dims(head_dim=96)) == (0, 0)
