@@ -31,12 +31,13 @@ namespace ppa {
 
 template <int D>
 struct PairCfg {
-  static_assert(D == 256, "the pair kernel serves head_dim 256");
+  static_assert(D == 128 || D == 256, "the pair kernel serves head_dim 128 and 256");
   static constexpr int M = kRowsPerTile;  // rows per CTA (one query tile)
   static constexpr int TN = 128;          // keys per key tile
   static constexpr int KH = TN / 2;       // K rows held by each CTA
   static constexpr int DH = D / 2;        // V columns held by each CTA
-  static constexpr int NSK = 3, NSV = 2;  // K and V stages
+  static constexpr int NSK = D == 256 ? 3 : 4;  // K stages
+  static constexpr int NSV = D == 256 ? 2 : 4;  // V stages
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int KS_BYTES = KH * D * 2;   // one K stage: 64 rows x 256 columns
   static constexpr int VS_BYTES = TN * DH * 2;  // one V stage: 128 rows x 128 columns

@@ -44,26 +44,22 @@ namespace ppa {
 
 template <int D>
 struct WsCfg {
-  static_assert(D == 64 || D == 128 || D == 256, "head_dim 64, 128 or 256");
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128 (256 runs on CTA pairs)");
   static constexpr int M = kRowsPerTile;  // rows per query tile
-  // D <= 128: two query tiles share each 128-key tile (S_A, S_B, O_A, O_B fill TMEM).
-  // D = 256: one query tile (O takes 256 columns) with a double-buffered S of 64-key tiles.
-  static constexpr int NQ = D <= 128 ? 2 : 1;  // query tiles per unit
-  static constexpr int TN = D <= 128 ? 128 : 64;  // keys per key tile
-  static constexpr int NSB = NQ == 2 ? 1 : 2;  // S buffers per query tile
-  // K and V rings: D = 256 keeps a third K stage so that K(kt+2) is resident by the time the
-  // softmax of tile kt certifies it (the single-tile issuer waits on P alone).
-  static constexpr int NSK = D == 64 ? 4 : (D == 256 ? 3 : 2);  // K stages
-  static constexpr int NSV = D == 64 ? 4 : 2;                    // V stages
+  // Two query tiles share each 128-key tile (S_A, S_B, O_A, O_B fill TMEM).
+  static constexpr int NQ = 2;    // query tiles per unit
+  static constexpr int TN = 128;  // keys per key tile
+  static constexpr int NSB = 1;   // S buffers per query tile
+  static constexpr int NSK = D == 64 ? 4 : 2;  // K stages
+  static constexpr int NSV = NSK;              // V stages
   static constexpr int CPR = D / 8;       // 16-byte chunks per bf16 row
   static constexpr int Q_BYTES = M * D * 2;
   static constexpr int KV_BYTES = TN * D * 2;
   static constexpr int Q_OFF = 0;
-  // K stage s at KV_OFF + s*STAGE_STRIDE, V stage s at V_OFF + s*STAGE_STRIDE: interleaved
-  // (K, V, K, V, ...) when both rings have the same depth, two separate rings otherwise.
+  // K stage s at KV_OFF + s*STAGE_STRIDE, V stage s at V_OFF + s*STAGE_STRIDE (interleaved)
   static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;
-  static constexpr int STAGE_STRIDE = NSK == NSV ? 2 * KV_BYTES : KV_BYTES;
-  static constexpr int V_OFF = NSK == NSV ? KV_OFF + KV_BYTES : KV_OFF + NSK * KV_BYTES;
+  static constexpr int STAGE_STRIDE = 2 * KV_BYTES;
+  static constexpr int V_OFF = KV_OFF + KV_BYTES;
   static constexpr int BAR_OFF = KV_OFF + (NSK + NSV) * KV_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;  // + alignment slack
@@ -531,101 +527,6 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   }
 }
 
-// MMA role for one query tile per unit (D = 256): S is double-buffered, so S(kt+1) is issued
-// before PV(kt) and the softmax of tile kt overlaps both. One commit to O_DONE per PV lets the
-// softmax know when O is idle (for a rescale) and when it is final (epilogue).
-template <int D>
-__device__ void ws_mma_single(const AttnParams& p, const WsShared& sh, uint32_t base,
-                              uint32_t tmem) {
-  using C = WsCfg<D>;
-  if ((threadIdx.x & 31) != 0) return;
-  constexpr uint32_t kIdescS = idesc_bf16_f32(128, C::TN, false, false);
-  constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, false, true);
-  uint32_t kv_iter = 0, q_phase = 0, pf_phase = 0, oe_phase = 0, sc = 0;
-  const uint64_t dQ = sdesc_sw128(base + C::Q_OFF, 16, 1024);
-  const uint64_t dK0 = sdesc_sw128(base + C::KV_OFF, 16, 1024);
-  const uint64_t dV0 = sdesc_sw128(base + C::V_OFF, C::TN * 128, 1024);
-  constexpr uint32_t kStageStep = C::STAGE_STRIDE >> 4;
-  constexpr int NSK = C::NSK, NSV = C::NSV;
-  auto issue_s = [&](int stage, uint32_t buf) {
-    const uint32_t tS = tmem + C::TM_S + buf * C::TN;
-    uint64_t a0 = dQ, b0 = dK0 + stage * kStageStep;
-    asm volatile("" : "+l"(a0), "+l"(b0));  // keep per-MMA descriptors out of registers
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off_a = ((kk >> 2) * (C::M * 128) + (kk & 3) * 32) >> 4;
-      const uint32_t off_b = ((kk >> 2) * (C::TN * 128) + (kk & 3) * 32) >> 4;
-      mma_bf16_ss(tS, a0 + off_a, b0 + off_b, kIdescS, kk > 0 ? 1u : 0u);
-    }
-    tc_commit(sh.bar(wsbar::S_FULL + 8 * buf));
-  };
-  bool ok = true;
-  for (int k = 0; ok; ++k) {
-    const int item = ring_get1(sh, k);
-    if (item < 0) break;
-    const UnitInfo u = decode_item(p, item);
-    if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
-    q_phase ^= 1;
-    tc_fence_after();
-    auto issue_pv = [&](int stage, uint32_t buf, uint32_t acc0) {
-      const uint32_t tP = tmem + C::TM_S + buf * C::TN;
-      uint64_t b0 = dV0 + stage * kStageStep;
-      asm volatile("" : "+l"(b0));
-#pragma unroll
-      for (int kk = 0; kk < C::TN / 16; ++kk)
-        mma_bf16_ts(tmem + C::TM_O, tP + kk * 8, b0 + ((kk * 16 * 128) >> 4), kIdescO,
-                    kk > 0 ? 1u : acc0);
-      tc_commit(sh.bar(wsbar::O_DONE));
-      tc_commit(sh.bar(wsbar::V_EMPTY + 8 * stage));
-    };
-    for (int kt = u.lo; kt < u.hi && ok;) {
-      // Steady state (not the first key tile, a next one exists): straight-line code, two
-      // waits per key tile. P(kt) also certifies V(kt): the softmax waited for it.
-      // Steady state (kt > lo, a next tile exists): S(kt+1) needs K(kt+1), which P(kt-1)
-      // certified (kt+1 >= lo+2), so the only wait per key tile is P(kt).
-      if (kt > u.lo && kt + 1 < u.hi) {
-        for (; kt + 1 < u.hi; ++kt, ++kv_iter, ++sc) {
-          const int sv = kv_iter % NSV, s2 = (kv_iter + 1) % NSK;
-          issue_s(s2, (sc + 1) & 1);
-          tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
-          if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }
-          pf_phase ^= 1;
-          tc_fence_after();
-          issue_pv(sv, sc & 1, 1u);
-        }
-        continue;
-      }
-      const int sk = kv_iter % NSK, sv = kv_iter % NSV;
-      if (kt == u.lo) {  // the unit's first two S: no P certifies their K yet
-        if (!sh.wait(wsbar::K_FULL + 8 * sk, (kv_iter / NSK) & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_s(sk, sc & 1);
-        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * sk));  // S(kt) is K(kt)'s only reader
-      }
-      if (kt == u.hi - 1) tc_commit(sh.bar(wsbar::Q_EMPTY));  // every S issued: free Q early
-      if (kt + 1 < u.hi) {
-        const int s2 = (kv_iter + 1) % NSK;
-        if (kt == u.lo &&
-            !sh.wait(wsbar::K_FULL + 8 * s2, ((kv_iter + 1) / NSK) & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_s(s2, (sc + 1) & 1);
-        tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s2));
-      }
-      if (kt == u.lo) {  // O must have been read out by the previous epilogue
-        if (!sh.wait(wsbar::O_EMPTY, oe_phase ^ 1)) { ok = false; break; }
-        oe_phase ^= 1;
-      }
-      if (!sh.wait(wsbar::P_FULL, pf_phase)) { ok = false; break; }  // certifies V(kt)
-      pf_phase ^= 1;
-      tc_fence_after();
-      issue_pv(sv, sc & 1, kt > u.lo ? 1u : 0u);
-      ++kv_iter;
-      ++sc;
-      ++kt;
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------------------
 // Softmax role (warps 0-7): warpgroup i owns query tile i; thread r owns row r.
 // ---------------------------------------------------------------------------------------
@@ -639,9 +540,8 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
   const uint32_t tO = tmem + C::TM_O + i * D + lane_off;
   const float neg_inf = -__int_as_float(0x7f800000);
   const float scale = p.scale_log2;
-  // NQ == 2: one S buffer per tile, S_FULL[i] and O_DONE[i] flip once per use.
-  // NQ == 1: S buffers alternate (tile count sc), O_DONE completes once per PV.
-  uint32_t sf_phase = 0, od_phase = 0, sc = 0;
+  // One S buffer per tile: S_FULL[i] and O_DONE[i] flip once per use.
+  uint32_t sf_phase = 0, od_phase = 0;
   uint32_t kv_next = 0;  // K/V ring position of the next unit's first key tile
   for (int k = 0;; ++k) {
     const int item = ring_get(sh, k);
@@ -668,34 +568,20 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     float m_ref = neg_inf, l_run = 0.f;
     bool ok = true;
     for (int kt = lo; kt < hi; ++kt) {
-      const uint32_t buf = C::NQ == 2 ? 0u : (sc & 1);
-      const uint32_t tS = tmem + C::TM_S + (i * C::NSB + buf) * C::TN + lane_off;
+      const uint32_t tS = tmem + C::TM_S + i * C::TN + lane_off;
       const uint32_t kv = kv0 + (kt - u.lo);  // ring position of key tile kt
-      // K certified with P(kt): K(kt+1) for two-tile units (S(kt+1) follows PV(kt)), K(kt+2)
-      // for one-tile units (S(kt+2) is issued after P(kt) is seen, before PV(kt+1)).
-      constexpr uint32_t kAhead = C::NQ == 2 ? 1 : 2;
       const uint32_t bar_v = wsbar::V_FULL + 8 * (kv % C::NSV), par_v = (kv / C::NSV) & 1;
-      const uint32_t bar_k = wsbar::K_FULL + 8 * ((kv + kAhead) % C::NSK);
-      const uint32_t par_k = ((kv + kAhead) / C::NSK) & 1;
-      bool v_ready = true, k_ready = true;
-      if constexpr (C::NQ == 2) {
-        if (!wait_warp(sh, wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
-        sf_phase ^= 1;
-        // V(kt) and K(kt+1) must be resident before P_FULL lets the issuer start PV(kt) and
-        // S(kt+1). Probe both now (non-blocking; the latency overlaps the softmax) and wait
-        // before the arrival only for what was not ready. Probing after S(kt) has landed
-        // is what makes the parity test unambiguous: every earlier fill of these stages that
-        // a tile uses was confirmed before the issuer could issue S(kt).
-        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);
-        k_ready = kt + 1 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
-      } else {
-        if (!wait_warp(sh, wsbar::S_FULL + 8 * buf, (sc >> 1) & 1)) { ok = false; break; }
-        // Same reasoning. The previous fill of K(kt+2)'s stage, K(kt-1), was confirmed
-        // before S(kt-1), hence before S(kt).
-        v_ready = mbar_test_wait(sh.bar(bar_v), par_v);
-        k_ready = kt + 2 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
-      }
-      ++sc;
+      const uint32_t bar_k = wsbar::K_FULL + 8 * ((kv + 1) % C::NSK);
+      const uint32_t par_k = ((kv + 1) / C::NSK) & 1;
+      if (!wait_warp(sh, wsbar::S_FULL + 8 * i, sf_phase)) { ok = false; break; }
+      sf_phase ^= 1;
+      // V(kt) and K(kt+1) must be resident before P_FULL lets the issuer start PV(kt) and
+      // S(kt+1). Probe both now (non-blocking; the latency overlaps the softmax) and wait
+      // before the arrival only for what was not ready. Probing after S(kt) has landed is
+      // what makes the parity test unambiguous: every earlier fill of these stages that a
+      // tile uses was confirmed before the issuer could issue S(kt).
+      const bool v_ready = mbar_test_wait(sh.bar(bar_v), par_v);
+      const bool k_ready = kt + 1 >= hi || mbar_test_wait(sh.bar(bar_k), par_k);
       tc_fence_after();
       float sv[C::TN];
 #pragma unroll
@@ -771,15 +657,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         for (int e = 0; e < 32; ++e) w32[e] = pk[cc * 32 + e];
         tmem_st_32(tS + cc * 32, w32);
       }
-      // NQ == 2: O_i is idle here, PV_i(kt-1) completed before S_i(kt) (one issuing thread,
-      // in order). NQ == 1: S(kt) was issued before PV(kt-1), so wait for that PV first.
-      if constexpr (C::NQ == 1) {
-        if (kt > lo) {
-          if (!wait_warp(sh, wsbar::O_DONE, od_phase)) { ok = false; break; }
-          od_phase ^= 1;
-          tc_fence_after();
-        }
-      }
+      // O_i is idle here: PV_i(kt-1) completed before S_i(kt) (one issuing thread, in order).
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -884,11 +762,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     } else if (warp == 13) {
       ws_qloader<D>(p, sh, base, n_items);
     } else if (warp == 12) {
-      if constexpr (C::NQ == 2) {
-        ws_mma<D>(p, sh, base, tmem);
-      } else {
-        ws_mma_single<D>(p, sh, base, tmem);
-      }
+      ws_mma<D>(p, sh, base, tmem);
       if ((tid & 31) == 0) {  // retire every MMA this CTA issued before TMEM is freed
         tc_commit(sh.bar(wsbar::FIN));
         const uint64_t t0 = globaltimer_ns();
