@@ -58,6 +58,14 @@ def make_workload(name: str, seed: int):
     if name == "mixed":
         return ("mixed serving: 32 seqs, ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, "
                 "D 128, causal, page 544, no window, bf16 KV", [wl.mixed(544, False, seed=seed)])
+    if name == "mixed_fp8":
+        return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
+                "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
+                [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
+    if name == "mixed_window":
+        return ("mixed serving with window_left 4096: 32 seqs, ctx U[4096,32768], q U[512,4096], "
+                "32 q / 4 kv heads, D 128, causal, page 2048, bf16 KV",
+                [wl.mixed(2048, True, seed=seed)])
     raise SystemExit(f"unknown workload {name}")
 
 

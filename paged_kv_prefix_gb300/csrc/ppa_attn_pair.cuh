@@ -298,8 +298,17 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
           } else if (pos < u.s) {
             mine = g_new + (((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D + col0) * 2;
           }
-          pair_gather_rows<FP8>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
-                                mine, sX, rows, ncol_blocks * 64);
+          if constexpr (FP8) {
+            if (w == 0)
+              gather_rows_fp8<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
+                                 mine, sX, rows);
+            else
+              gather_rows_fp8<C::DH>(static_cast<const char*>(p.k_new), row0, fb_mask,
+                                     u.c - p_row0, mine, sX, rows);
+          } else {
+            pair_gather_rows<FP8>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
+                                  mine, sX, rows, ncol_blocks * 64);
+          }
           any_fallback = true;
         }
       }

@@ -200,6 +200,42 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 // its boxes.
 // ---------------------------------------------------------------------------------------
 
+// Gather of one 32-row block with an fp8 cache, one row per lane: lane r sources row
+// row0 + r (if its bit is set in `rowmask`) from `mine` (nullptr: zero fill). Rows below
+// `cache_rows` are fp8 cache rows of COLS codes: the lane issues all its 16-byte loads first,
+// so their latency overlaps, then widens them to bf16. Later rows are bf16 new tokens, copied
+// with cp.async. `rows` is the number of rows per 64-column block of the destination.
+template <int COLS>
+__device__ __forceinline__ void gather_rows_fp8(const char* zero_src, int row0, uint32_t rowmask,
+                                                int cache_rows, const char* mine, uint32_t sX,
+                                                int rows) {
+  const int lane = threadIdx.x & 31;
+  if (!((rowmask >> lane) & 1u)) return;
+  const int row = row0 + lane;
+  if (lane < cache_rows) {
+    uint4 codes[COLS / 16];
+#pragma unroll
+    for (int un = 0; un < COLS / 16; ++un)
+      codes[un] = mine ? ld_global_nc_v4(mine + un * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int un = 0; un < COLS / 16; ++un) {
+      const uint32_t cw[4] = {codes[un].x, codes[un].y, codes[un].z, codes[un].w};
+      uint32_t v[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        v[2 * q4] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] & 0xFFFFu));
+        v[2 * q4 + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] >> 16));
+      }
+      st_shared_v4(sX + swz128(row, 2 * un, rows), v[0], v[1], v[2], v[3]);
+      st_shared_v4(sX + swz128(row, 2 * un + 1, rows), v[4], v[5], v[6], v[7]);
+    }
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < COLS / 8; ++ch)
+      cp_async_16(sX + swz128(row, ch, rows), mine ? mine + ch * 16 : zero_src, mine ? 16u : 0u);
+  }
+}
+
 // Row-wise gather of rows row0 .. row0+nrows-1 whose bit is set in `rowmask`; `mine` is the
 // source row of lane `lane` (lanes >= nrows unused), nullptr for zero fill.
 template <int D, bool FP8>
@@ -363,7 +399,12 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
           } else if (pos < u.s) {
             mine = g_new + ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D * 2;
           }
-          gather_rows<D, FP8>(p, row0, 32, fb_mask, u.c - p_row0, mine, sX);
+          if constexpr (FP8) {
+            gather_rows_fp8<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0, mine,
+                               sX, C::TN);
+          } else {
+            gather_rows<D, FP8>(p, row0, 32, fb_mask, u.c - p_row0, mine, sX);
+          }
           any_fallback = true;
         }
       }
