@@ -126,56 +126,22 @@ __device__ __forceinline__ void pair_ring_put(const PairShared& sh, const AttnPa
   mbar_arrive_cluster(mapa_shared(sh.bar(wsbar::ITEM_FULL + 8 * slot), 1));
 }
 
-// Row gather for one 32-row block: rows row0 .. row0+31 whose bit is set in `rowmask`; lane
-// l's source row starts at `mine` (nullptr: zero fill); `cols` elements per row land in the
-// 128-byte-swizzled layout with `rows` rows per 64-column block. With an fp8 cache, the first
-// `cache_rows` rows of the block are fp8 cache rows (widened here); the rest are bf16 new
-// tokens, copied as they are.
-template <bool FP8>
+// Row gather (bf16 cache) for one 32-row block: rows row0 .. row0+31 whose bit is set in
+// `rowmask`; lane l's source row starts at `mine` (nullptr: zero fill); `cols` elements per
+// row land in the 128-byte-swizzled layout with `rows` rows per 64-column block.
 __device__ __forceinline__ void pair_gather_rows(const char* zero_src, int row0, uint32_t rowmask,
-                                                 int cache_rows, const char* mine, uint32_t sX,
-                                                 int rows, int cols) {
+                                                 const char* mine, uint32_t sX, int rows,
+                                                 int cols) {
   const int lane = threadIdx.x & 31;
-  if constexpr (!FP8) {
-    const int cpr = cols / 8;  // 16-byte chunks per row
-    const int rpi = 32 / cpr;  // rows per warp instruction
-    for (int it = 0; it * rpi < 32; ++it) {
-      const int lr = it * rpi + lane / cpr;
-      const int ch = lane % cpr;
-      const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
-      if (lr < 32 && ((rowmask >> lr) & 1u))
-        cp_async_16(sX + swz128(row0 + lr, ch, rows), rp ? rp + ch * 16 : zero_src,
-                    rp ? 16u : 0u);
-    }
-  } else {
-    const int upr = cols / 16;  // 16-element units per row (16 source bytes, 32 bytes here)
-    const int rpu = 32 / upr;
-    for (int it = 0; it * rpu < 32; ++it) {
-      const int lr = it * rpu + lane / upr;
-      const int un = lane % upr;
-      const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
-      if (!(lr < 32 && ((rowmask >> lr) & 1u))) continue;
-      const uint32_t o0 = swz128(row0 + lr, 2 * un, rows), o1 = swz128(row0 + lr, 2 * un + 1, rows);
-      if (lr < cache_rows) {
-        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (rp) {
-          const uint4 codes = ld_global_nc_v4(rp + un * 16);
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            v[2 * q4] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] & 0xFFFFu));
-            v[2 * q4 + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] >> 16));
-          }
-        }
-        st_shared_v4(sX + o0, v[0], v[1], v[2], v[3]);
-        st_shared_v4(sX + o1, v[4], v[5], v[6], v[7]);
-      } else {  // bf16 new-token row: 32 bytes per 16-element unit
-        cp_async_16(sX + o0, rp ? rp + un * 32 : zero_src, rp ? 16u : 0u);
-        cp_async_16(sX + o1, rp ? rp + un * 32 + 16 : zero_src, rp ? 16u : 0u);
-      }
-    }
+  const int cpr = cols / 8;  // 16-byte chunks per row
+  const int rpi = 32 / cpr;  // rows per warp instruction
+  for (int it = 0; it * rpi < 32; ++it) {
+    const int lr = it * rpi + lane / cpr;
+    const int ch = lane % cpr;
+    const char* rp = reinterpret_cast<const char*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
+    if (lr < 32 && ((rowmask >> lr) & 1u))
+      cp_async_16(sX + swz128(row0 + lr, ch, rows), rp ? rp + ch * 16 : zero_src, rp ? 16u : 0u);
   }
 }
 
@@ -216,6 +182,7 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
   const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
   const int full_bar = w == 0 ? wsbar::K_FULL : wsbar::V_FULL;
   const uint32_t stage0 = base + (w == 0 ? C::K_OFF : C::V_OFF);
+  const float kv_scale = FP8 ? *(w == 0 ? p.k_scale : p.v_scale) : 1.f;  // fp8 dequantisation
   const uint32_t stage_bytes = w == 0 ? C::KS_BYTES : C::VS_BYTES;
   uint32_t kv_iter = 0;
   for (int k = 0;; ++k) {
@@ -301,13 +268,13 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
           if constexpr (FP8) {
             if (w == 0)
               gather_rows_fp8<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
-                                 mine, sX, rows);
+                                 mine, sX, rows, kv_scale);
             else
               gather_rows_fp8<C::DH>(static_cast<const char*>(p.k_new), row0, fb_mask,
-                                     u.c - p_row0, mine, sX, rows);
+                                     u.c - p_row0, mine, sX, rows, kv_scale);
           } else {
-            pair_gather_rows<FP8>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
-                                  mine, sX, rows, ncol_blocks * 64);
+            pair_gather_rows(static_cast<const char*>(p.k_new), row0, fb_mask, mine, sX, rows,
+                             ncol_blocks * 64);
           }
           any_fallback = true;
         }
@@ -494,11 +461,6 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
           p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)u.b * p.mask.max_mm_ranges * 2 : nullptr;
       row_interval(u.c + j, u.s, p.mask, ranges, kmin, kmax);
     }
-    float ks_ctx = 1.f, vs_ctx = 1.f;
-    if constexpr (FP8) {
-      ks_ctx = *p.k_scale;
-      vs_ctx = *p.v_scale;
-    }
     float m_ref = neg_inf, l_run = 0.f;
     bool ok = true;
     for (int kt = lo; kt < hi; ++kt) {
@@ -521,11 +483,6 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
         for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
       }
       const int k0 = kt * C::TN;
-      if constexpr (FP8) {  // cache columns carry the K dequantisation scale
-        const int jc = min(max(u.c - k0, 0), C::TN);
-#pragma unroll
-        for (int e = 0; e < C::TN; ++e) sv[e] = e < jc ? sv[e] * ks_ctx : sv[e];
-      }
       const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
       if (!(a0 <= 0 && a1 >= C::TN - 1)) {
 #pragma unroll
@@ -563,11 +520,6 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
         float p0 = ex2_approx(y0);
         float p1 = ex2_approx(y1);
         sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-        if constexpr (FP8) {
-          const int jc = min(max(u.c - k0, 0), C::TN);
-          p0 = e < jc ? p0 * vs_ctx : p0;
-          p1 = e + 1 < jc ? p1 * vs_ctx : p1;
-        }
         pk[e >> 1] = pack_bf16x2(p0, p1);
       }
       float sl[8];

@@ -60,7 +60,11 @@ struct WsCfg {
   static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int STAGE_STRIDE = 2 * KV_BYTES;
   static constexpr int V_OFF = KV_OFF + KV_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + (NSK + NSV) * KV_BYTES;
+  // fp8 caches: per producer warp, a staging area for its 64 rows of raw e4m3 bytes
+  static constexpr int STG_OFF = KV_OFF + (NSK + NSV) * KV_BYTES;
+  static constexpr int STG_ROWS = TN / 2;  // rows per producer warp
+  static constexpr int STG_BYTES = 4 * STG_ROWS * D;
+  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int TM_O = 0;       // O_i at column TM_O + i*D
@@ -200,6 +204,56 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 // its boxes.
 // ---------------------------------------------------------------------------------------
 
+// fp8 cache, first half of a 32-row block's gather (one row per lane): the lane copies its
+// row's raw e4m3 bytes (rows below `cache_rows`) into its staging row with cp.async, or its
+// bf16 new-token row straight into the stage. No registers hold the data, so all rows of the
+// warp are in flight at once; fp8_stage_widen() finishes the cache rows.
+template <int D>
+__device__ __forceinline__ void fp8_stage_issue(const char* zero_src, int row0, uint32_t rowmask,
+                                                int cache_rows, const char* mine, uint32_t sX,
+                                                int rows, uint32_t stg_row) {
+  const int lane = threadIdx.x & 31;
+  if (!((rowmask >> lane) & 1u)) return;
+  if (lane < cache_rows) {
+    // 16-byte pieces at position un ^ (lane mod D/16): the widening reads stay free of bank
+    // conflicts although every lane's row starts at the same bank
+#pragma unroll
+    for (int un = 0; un < D / 16; ++un)
+      cp_async_16(stg_row + ((un ^ lane) & (D / 16 - 1)) * 16, mine ? mine + un * 16 : zero_src,
+                  mine ? 16u : 0u);
+  } else {
+#pragma unroll
+    for (int ch = 0; ch < D / 8; ++ch)
+      cp_async_16(sX + swz128(row0 + lane, ch, rows), mine ? mine + ch * 16 : zero_src,
+                  mine ? 16u : 0u);
+  }
+}
+
+// Second half: widen the lane's staged e4m3 row to bf16 into the 128-byte-swizzled stage,
+// times the tensor's dequantisation scale (so no later step has to tell cache keys from new
+// ones: the product decode(code) * scale is rounded once, to bf16).
+template <int D>
+__device__ __forceinline__ void fp8_stage_widen(int row0, uint32_t rowmask, int cache_rows,
+                                                uint32_t sX, int rows, uint32_t stg_row,
+                                                float scale) {
+  const int lane = threadIdx.x & 31;
+  if (!((rowmask >> lane) & 1u) || lane >= cache_rows) return;
+  const int row = row0 + lane;
+#pragma unroll
+  for (int un = 0; un < D / 16; ++un) {
+    const uint4 codes = ld_shared_v4(stg_row + ((un ^ lane) & (D / 16 - 1)) * 16);
+    const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint32_t v[8];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      v[2 * q4] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] & 0xFFFFu), scale);
+      v[2 * q4 + 1] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] >> 16), scale);
+    }
+    st_shared_v4(sX + swz128(row, 2 * un, rows), v[0], v[1], v[2], v[3]);
+    st_shared_v4(sX + swz128(row, 2 * un + 1, rows), v[4], v[5], v[6], v[7]);
+  }
+}
+
 // Gather of one 32-row block with an fp8 cache, one row per lane: lane r sources row
 // row0 + r (if its bit is set in `rowmask`) from `mine` (nullptr: zero fill). Rows below
 // `cache_rows` are fp8 cache rows of COLS codes: the lane issues all its 16-byte loads first,
@@ -208,7 +262,7 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 template <int COLS>
 __device__ __forceinline__ void gather_rows_fp8(const char* zero_src, int row0, uint32_t rowmask,
                                                 int cache_rows, const char* mine, uint32_t sX,
-                                                int rows) {
+                                                int rows, float scale) {
   const int lane = threadIdx.x & 31;
   if (!((rowmask >> lane) & 1u)) return;
   const int row = row0 + lane;
@@ -223,8 +277,8 @@ __device__ __forceinline__ void gather_rows_fp8(const char* zero_src, int row0, 
       uint32_t v[8];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        v[2 * q4] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] & 0xFFFFu));
-        v[2 * q4 + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] >> 16));
+        v[2 * q4] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] & 0xFFFFu), scale);
+        v[2 * q4 + 1] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] >> 16), scale);
       }
       st_shared_v4(sX + swz128(row, 2 * un, rows), v[0], v[1], v[2], v[3]);
       st_shared_v4(sX + swz128(row, 2 * un + 1, rows), v[4], v[5], v[6], v[7]);
@@ -236,55 +290,22 @@ __device__ __forceinline__ void gather_rows_fp8(const char* zero_src, int row0, 
   }
 }
 
-// Row-wise gather of rows row0 .. row0+nrows-1 whose bit is set in `rowmask`; `mine` is the
-// source row of lane `lane` (lanes >= nrows unused), nullptr for zero fill.
-template <int D, bool FP8>
+// Row-wise gather (bf16 cache) of rows row0 .. row0+nrows-1 whose bit is set in `rowmask`;
+// `mine` is the source row of lane `lane` (lanes >= nrows unused), nullptr for zero fill.
+template <int D>
 __device__ __forceinline__ void gather_rows(const AttnParams& p, int row0, int nrows,
-                                            uint32_t rowmask, int cache_rows, const char* mine,
-                                            uint32_t sX) {
+                                            uint32_t rowmask, const char* mine, uint32_t sX) {
   using C = WsCfg<D>;
   const int lane = threadIdx.x & 31;
-  if constexpr (!FP8) {
-    constexpr int RPI = 32 / C::CPR;  // rows per warp instruction
-    for (int it = 0; it * RPI < nrows; ++it) {
-      const int lr = it * RPI + lane / C::CPR;
-      const int ch = lane % C::CPR;
-      const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
-      if (lr < nrows && ((rowmask >> lr) & 1u))
-        cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
-                    rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
-    }
-  } else {
-    constexpr int UPR = D / 16;    // 16-element units per row
-    constexpr int RPU = 32 / UPR;  // rows per warp instruction
-    for (int it = 0; it * RPU < nrows; ++it) {
-      const int lr = it * RPU + lane / UPR;
-      const int un = lane % UPR;
-      const char* rp = reinterpret_cast<const char*>(
-          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
-      if (!(lr < nrows && ((rowmask >> lr) & 1u))) continue;
-      const uint32_t o0 = swz128(row0 + lr, 2 * un, C::TN);
-      const uint32_t o1 = swz128(row0 + lr, 2 * un + 1, C::TN);
-      if (lr < cache_rows) {  // fp8 cache row: widen to bf16 here
-        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (rp) {
-          const uint4 codes = ld_global_nc_v4(rp + un * 16);
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            v[2 * q4] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] & 0xFFFFu));
-            v[2 * q4 + 1] = e4m3x2_to_bf16x2(static_cast<uint16_t>(cw[q4] >> 16));
-          }
-        }
-        st_shared_v4(sX + o0, v[0], v[1], v[2], v[3]);
-        st_shared_v4(sX + o1, v[4], v[5], v[6], v[7]);
-      } else {
-        const char* fb = static_cast<const char*>(p.k_new);
-        cp_async_16(sX + o0, rp ? rp + un * 32 : fb, rp ? 16u : 0u);
-        cp_async_16(sX + o1, rp ? rp + un * 32 + 16 : fb, rp ? 16u : 0u);
-      }
-    }
+  constexpr int RPI = 32 / C::CPR;  // rows per warp instruction
+  for (int it = 0; it * RPI < nrows; ++it) {
+    const int lr = it * RPI + lane / C::CPR;
+    const int ch = lane % C::CPR;
+    const char* rp = reinterpret_cast<const char*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
+    if (lr < nrows && ((rowmask >> lr) & 1u))
+      cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
+                  rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
   }
 }
 
@@ -315,6 +336,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   }
   const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
   const int full_bar = w == 0 ? wsbar::K_FULL : wsbar::V_FULL;
+  const float kv_scale = FP8 ? *(w == 0 ? p.k_scale : p.v_scale) : 1.f;  // fp8 dequantisation
   uint32_t kv_iter = 0;
   for (int k = 0;; ++k) {
     const int item = ring_get(sh, k);
@@ -351,8 +373,13 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       const uint32_t bar = sh.bar(full_bar + 8 * s);
       uint32_t bytes = 0;
       bool any_fallback = false;
+      uint32_t fp8_mask[NSUB];  // fp8: rows of each 32-row block still to widen
+      int fp8_cache_rows[NSUB];
+      const uint32_t stg = base + C::STG_OFF + pw * (C::STG_ROWS * D);  // this warp's staging
 #pragma unroll
       for (int sub = 0; sub < NSUB; ++sub) {
+        fp8_mask[sub] = 0;
+        fp8_cache_rows[sub] = 0;
         const int row0 = half * RPW + 32 * sub;
         const int p_row0 = kt * C::TN + row0;  // key position of this block's first row
         int types[2], rows[2];
@@ -400,15 +427,32 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
             mine = g_new + ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D * 2;
           }
           if constexpr (FP8) {
-            gather_rows_fp8<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0, mine,
-                               sX, C::TN);
+            fp8_stage_issue<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0, mine,
+                               sX, C::TN, stg + (32 * sub + lane) * D);
+            fp8_mask[sub] = fb_mask;
+            fp8_cache_rows[sub] = u.c - p_row0;
           } else {
-            gather_rows<D, FP8>(p, row0, 32, fb_mask, u.c - p_row0, mine, sX);
+            gather_rows<D>(p, row0, 32, fb_mask, mine, sX);
           }
           any_fallback = true;
         }
+        if constexpr (FP8) cp_async_commit();  // one group per 32-row block
       }
-      if (any_fallback) {
+      if constexpr (FP8) {
+        // widen block 0 while block 1's copies are still landing
+        static_assert(NSUB == 2, "two 32-row blocks per producer warp");
+#pragma unroll
+        for (int sub = 0; sub < NSUB; ++sub) {
+          if (sub == 0) cp_async_wait<1>(); else cp_async_wait<0>();
+          if (fp8_mask[sub] != 0)
+            fp8_stage_widen<D>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub], sX, C::TN,
+                               stg + (32 * sub + lane) * D, kv_scale);
+        }
+        if (any_fallback) {
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+      } else if (any_fallback) {
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
@@ -601,11 +645,6 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
           p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)u.b * p.mask.max_mm_ranges * 2 : nullptr;
       row_interval(u.c + j, u.s, p.mask, ranges, kmin, kmax);
     }
-    float ks_ctx = 1.f, vs_ctx = 1.f;
-    if constexpr (FP8) {
-      ks_ctx = *p.k_scale;
-      vs_ctx = *p.v_scale;
-    }
     float m_ref = neg_inf, l_run = 0.f;
     bool ok = true;
     for (int kt = lo; kt < hi; ++kt) {
@@ -633,11 +672,6 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
       }
       const int k0 = kt * C::TN;
-      if constexpr (FP8) {  // cache columns carry the K dequantisation scale
-        const int jc = min(max(u.c - k0, 0), C::TN);
-#pragma unroll
-        for (int e = 0; e < C::TN; ++e) sv[e] = e < jc ? sv[e] * ks_ctx : sv[e];
-      }
       const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
       if (!(a0 <= 0 && a1 >= C::TN - 1)) {
 #pragma unroll
@@ -678,11 +712,6 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         float p0 = ex2_approx(y0);
         float p1 = ex2_approx(y1);
         sum2[(e >> 1) & 3] = f2_add(sum2[(e >> 1) & 3], f2_pack(p0, p1));
-        if constexpr (FP8) {
-          const int jc = min(max(u.c - k0, 0), C::TN);
-          p0 = e < jc ? p0 * vs_ctx : p0;
-          p1 = e + 1 < jc ? p1 * vs_ctx : p1;
-        }
         pk[e >> 1] = pack_bf16x2(p0, p1);
       }
       float sl[8];
