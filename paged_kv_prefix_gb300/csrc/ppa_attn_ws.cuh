@@ -82,7 +82,7 @@ namespace wsbar {
 constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL = 48,
               V_FULL = 80, K_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
               O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224,
-              V_EMPTY = 240;
+              V_EMPTY = 240, FOLD = 288;  // FOLD: fp8 scale constants, see Fp8Fold
 constexpr int kRingConsumers = 14;  // warps 0..13 each release a ring slot once
 }  // namespace wsbar
 
@@ -204,6 +204,32 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch, int rows) {
 // its boxes.
 // ---------------------------------------------------------------------------------------
 
+// Where an fp8 cache's dequantisation scales are applied. With `fold` (the usual case) a
+// producer widens a cache row to bf16(decode(code)) * 2^-112 (exact, e4m3x2_to_bf16x2_m112)
+// and the softmax applies the scales: on a key tile made only of cache rows the K scale joins
+// the row's exp2 multiplier and the V scale joins the exp2 argument as log2(v_scale * 2^112),
+// so P carries it into PV. A tile that also holds new tokens is widened with its scales, as
+// without folding, so the softmax only tells cache-only tiles from the rest. The bounds keep
+// every intermediate finite: scale_log2 * k_scale
+// * 2^112 and P * v_scale * 2^112 (P <= 2^8) stay below 2^127. Other scales (non-positive,
+// NaN, or too large) are applied by the producer, which then writes bf16(decode * scale).
+struct Fp8Fold {
+  bool fold;
+  float ks;      // k_scale * 2^112: data-domain S -> logit
+  float lv;      // log2(v_scale * 2^112)
+  float inv_vs;  // 1 / (v_scale * 2^112)
+};
+
+__device__ __forceinline__ Fp8Fold fp8_fold(const AttnParams& p) {
+  const float k = *p.k_scale, v = *p.v_scale;
+  Fp8Fold f;
+  f.fold = k > 0.f && v > 0.f && v < 0x1p7f && k < 0x1p15f && k * p.scale_log2 < 0x1p15f;
+  f.ks = k * 0x1p112f;
+  f.lv = log2f(v) + 112.f;
+  f.inv_vs = 1.f / (v * 0x1p112f);
+  return f;
+}
+
 // fp8 cache, first half of a 32-row block's gather (one row per lane): the lane copies its
 // row's raw e4m3 bytes (rows below `cache_rows`) into its staging row with cp.async, or its
 // bf16 new-token row straight into the stage. No registers hold the data, so all rows of the
@@ -229,10 +255,10 @@ __device__ __forceinline__ void fp8_stage_issue(const char* zero_src, int row0, 
   }
 }
 
-// Second half: widen the lane's staged e4m3 row to bf16 into the 128-byte-swizzled stage,
-// times the tensor's dequantisation scale (so no later step has to tell cache keys from new
-// ones: the product decode(code) * scale is rounded once, to bf16).
-template <int D>
+// Second half: widen the lane's staged e4m3 row to bf16 into the 128-byte-swizzled stage:
+// bf16(decode(code)) * 2^-112 when the softmax applies the scales (FOLD), else
+// bf16(decode(code) * scale), the fp32 product rounded once.
+template <int D, bool FOLD>
 __device__ __forceinline__ void fp8_stage_widen(int row0, uint32_t rowmask, int cache_rows,
                                                 uint32_t sX, int rows, uint32_t stg_row,
                                                 float scale) {
@@ -246,8 +272,10 @@ __device__ __forceinline__ void fp8_stage_widen(int row0, uint32_t rowmask, int 
     uint32_t v[8];
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
-      v[2 * q4] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] & 0xFFFFu), scale);
-      v[2 * q4 + 1] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] >> 16), scale);
+      const uint16_t c0 = static_cast<uint16_t>(cw[q4] & 0xFFFFu);
+      const uint16_t c1 = static_cast<uint16_t>(cw[q4] >> 16);
+      v[2 * q4] = FOLD ? e4m3x2_to_bf16x2_m112(c0) : e4m3x2_to_bf16x2_scaled(c0, scale);
+      v[2 * q4 + 1] = FOLD ? e4m3x2_to_bf16x2_m112(c1) : e4m3x2_to_bf16x2_scaled(c1, scale);
     }
     st_shared_v4(sX + swz128(row, 2 * un, rows), v[0], v[1], v[2], v[3]);
     st_shared_v4(sX + swz128(row, 2 * un + 1, rows), v[4], v[5], v[6], v[7]);
@@ -337,6 +365,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
   const int full_bar = w == 0 ? wsbar::K_FULL : wsbar::V_FULL;
   const float kv_scale = FP8 ? *(w == 0 ? p.k_scale : p.v_scale) : 1.f;  // fp8 dequantisation
+  const bool kv_fold = FP8 && fp8_fold(p).fold;
   uint32_t kv_iter = 0;
   for (int k = 0;; ++k) {
     const int item = ring_get(sh, k);
@@ -444,9 +473,14 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
 #pragma unroll
         for (int sub = 0; sub < NSUB; ++sub) {
           if (sub == 0) cp_async_wait<1>(); else cp_async_wait<0>();
-          if (fp8_mask[sub] != 0)
-            fp8_stage_widen<D>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub], sX, C::TN,
-                               stg + (32 * sub + lane) * D, kv_scale);
+          if (fp8_mask[sub] != 0) {
+            if (kv_fold && u.c >= (kt + 1) * C::TN)  // a cache-only tile: the softmax scales
+              fp8_stage_widen<D, true>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub],
+                                       sX, C::TN, stg + (32 * sub + lane) * D, kv_scale);
+            else
+              fp8_stage_widen<D, false>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub],
+                                        sX, C::TN, stg + (32 * sub + lane) * D, kv_scale);
+          }
         }
         if (any_fallback) {
           fence_proxy_async_smem();
@@ -672,6 +706,12 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
       }
       const int k0 = kt * C::TN;
+      // fp8 with folded scales: a tile of cache keys only was widened without its scales.
+      // The constants come from shared memory each tile (no registers held across tiles).
+      float2 fc = make_float2(0.f, 0.f);  // (scale_log2 * k_scale * 2^112, log2(v_scale * 2^112))
+      if constexpr (FP8) fc = ld_shared_f2(sh.bar(wsbar::FOLD));
+      const bool cache_tile = FP8 && fc.x != 0.f && u.c - k0 >= C::TN;
+      const float sc = cache_tile ? fc.x : scale;  // exp2 multiplier
       const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
       if (!(a0 <= 0 && a1 >= C::TN - 1)) {
 #pragma unroll
@@ -691,7 +731,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       }
       const float tile_max =
           fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      const float m_tile = tile_max * scale;  // in exp2 units
+      const float m_tile = tile_max * sc;  // in exp2 units
       // Keep the stale reference unless the maximum grew by more than 2^8.
       bool rescale = false;
       float alpha = 1.f;
@@ -701,8 +741,11 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
         m_ref = m_tile;
       }
       const float m_use = m_ref == neg_inf ? 0.f : m_ref;
-      // p = exp2(s * scale - m): the exponent arguments and the row sums run as packed pairs
-      const uint64_t scale2 = f2_pack(scale, scale), negm2 = f2_pack(-m_use, -m_use);
+      // p = exp2(s * sc - m): the exponent arguments and the row sums run as packed pairs. On
+      // an fp8 cache-only tile the argument also carries log2(v_scale * 2^112), so P is scaled
+      // for the PV MMA and its row sum is scaled back once.
+      const float lv = cache_tile ? fc.y : 0.f;
+      const uint64_t scale2 = f2_pack(sc, sc), negm2 = f2_pack(lv - m_use, lv - m_use);
       uint64_t sum2[4] = {0, 0, 0, 0};
       uint32_t pk[C::TN / 2];
 #pragma unroll
@@ -717,8 +760,9 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       float sl[8];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) f2_unpack(sum2[q4], sl[2 * q4], sl[2 * q4 + 1]);
-      l_run = l_run * alpha +
-              (((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7])));
+      float l_tile = ((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7]));
+      if (cache_tile) l_tile *= ld_shared_f32(sh.bar(wsbar::FOLD + 8));  // 1 / (v_scale 2^112)
+      l_run = l_run * alpha + l_tile;
       // P over the first TN/2 columns of this S buffer
 #pragma unroll
       for (int cc = 0; cc < C::TN / 64; ++cc) {
@@ -810,6 +854,13 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     }
     mbar_init(sh.bar(FIN), 1);
     *sh.abort = 0;
+    if constexpr (FP8) {
+      const Fp8Fold f = fp8_fold(p);
+      float* fc = reinterpret_cast<float*>(barp + FOLD);
+      fc[0] = f.fold ? p.scale_log2 * f.ks : 0.f;  // 0: scales not folded
+      fc[1] = f.lv;
+      fc[2] = f.inv_vs;
+    }
     fence_mbar_init();
   }
   if (warp == 0) {

@@ -98,6 +98,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Volatile, so a value kept in shared memory is reloaded where it is used instead of held in
+// a register across a loop.
+__device__ __forceinline__ float2 ld_shared_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -433,6 +446,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
       : "=f"(lo), "=f"(hi)
       : "r"(h2));
   return pack_bf16x2(lo, hi);
+}
+
+// Two e4m3fn codes -> packed bf16x2 of decode(code) * 2^-112, exactly. e4m3 -> f16 is exact
+// and lands on an f16 normal (or zero), whose low seven mantissa bits are zero; moving each
+// half's exponent and mantissa fields down by three bits leaves a bf16 whose 8-bit exponent
+// field holds the f16's 5-bit field unrebiased, i.e. the value times 2^(15 - 127).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_m112(uint16_t codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  return ((h2 & 0x7FFF7FFFu) >> 3) | (h2 & 0x80008000u);
 }
 
 // Two e4m3fn codes -> packed bf16x2 of decode(code) * scale (fp32 product, rounded once).

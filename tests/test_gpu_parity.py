@@ -81,6 +81,24 @@ def test_fp8_kv_head_dim_256(page, windowed):
                          window_left=100 if windowed else 0, kv_dtype="fp8_e4m3", seed=page))
 
 
+@pytest.mark.parametrize("head_dim", [128, 256])
+def test_fp8_kv_scales_of_2_8_and_above(head_dim):
+    """Dequantisation scales >= 2^8 take the widening's two-multiply branch (scale * 2^120
+    would overflow fp32). K's scale grows by 2^16 and the softmax scale shrinks by the same
+    power of two, so the logits keep their size; V's outputs grow by 2^16."""
+    import dataclasses
+    base = wl.build_case("fp8_big", [0, 200, 37], [50, 180, 9], 8, 2, head_dim, 37, causal=True,
+                         window_left=60, kv_dtype="fp8_e4m3", seed=31 + head_dim)
+    big = 2.0 ** 16
+    case = dataclasses.replace(base, k_scale=base.k_scale * big, v_scale=base.v_scale * big,
+                               sm_scale=head_dim ** -0.5 / big)
+    assert case.k_scale >= 256 and case.v_scale >= 256
+    got = run_gpu(case).out.float().cpu().numpy()
+    want = ref.attention(case.numpy_inputs())
+    # the tolerance applies at the outputs' own magnitude: compare both divided by 2^16
+    assert_close(got / big, want / big, case.name)
+
+
 def test_page_permutation_is_bitwise_invariant():
     a = wl.build_case("perm", [300, 1000], [200, 333], 8, 2, 128, 544, causal=True, seed=10,
                       value_rng_seed=77)
