@@ -72,6 +72,19 @@ def make_workload(name: str, seed: int):
 # ---------------------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------------------
+def _prepass(dc) -> bool:
+    """An fp8 cache dequantised into workspace before the attention kernel (the default)."""
+    from paged_kv_prefix_gb300 import binding
+    return (dc.dims.kv_dtype == binding.PPA_KV_FP8_E4M3
+            and not (dc.dims.flags & binding.PPA_FLAG_FP8_INKERNEL))
+
+
+def _launches_per_step(dc) -> int:
+    """Kernels of this library per step: the plan and the attention kernel, plus the fp8
+    live-tile marking and dequantisation kernels."""
+    return 2 + (2 if _prepass(dc) else 0)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -415,7 +428,9 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops"])
     roof = roofline(flops[dom], nbytes[dom], dom_avg_s, peaks, peak_src)
     roof["traffic"] = recorded_traffic(args.workload)
-    roof["kernel"] = f"attn_ws_kernel ({cases[dom].name})"
+    roof["kernel"] = (f"{'fp8 dequant + ' if _prepass(dcs[dom]) else ''}"
+                      f"{'attn_pair_kernel' if cases[dom].head_dim == 256 else 'attn_ws_kernel'} "
+                      f"({cases[dom].name})")
     shapes = []
     for i, case in enumerate(cases):
         a = float(attend_ms[:, i].mean())
@@ -450,7 +465,7 @@ def run_ours(args):
         "roofline": roof,
         "shapes": shapes,
         "e2e": e2e,
-        "gpu_launches": 2 * len(dcs) * args.steps,
+        "gpu_launches": sum(_launches_per_step(dc) for dc in dcs) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }

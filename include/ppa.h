@@ -72,7 +72,10 @@ enum { PPA_KV_BF16 = 0, PPA_KV_FP8_E4M3 = 1 };
 enum {
   PPA_FLAG_CAUSAL = 1u,   /* base mask is causal (k <= q); window_right is then ignored */
   PPA_FLAG_CLAMP_MM = 2u, /* multimodal keys also obey the left window (q - k < window_left) */
-  PPA_FLAG_NO_PRUNE = 4u  /* testing: visit every key tile 0 .. ceil(s/TN)-1 and mask them */
+  PPA_FLAG_NO_PRUNE = 4u, /* testing: visit every key tile 0 .. ceil(s/TN)-1 and mask them */
+  PPA_FLAG_FP8_INKERNEL = 8u /* fp8 caches: widen e4m3 rows inside the attention kernel instead
+                              * of dequantising the live cache tiles into workspace first; the
+                              * workspace then needs no bf16 scratch (ignored for bf16 caches) */
 };
 
 typedef struct {
@@ -93,6 +96,12 @@ typedef struct {
 } ppa_dims;
 
 /* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list).
+ * For an fp8 cache without PPA_FLAG_FP8_INKERNEL it also holds the bf16 scratch that the live
+ * cache key tiles are dequantised into before the attention kernel runs: room for
+ * num_seqs * ceil(max_pages_per_seq * page_size / 128) tiles of 128 positions for K and for
+ * V (2 * 128 * num_kv_heads * head_dim * 2 bytes per tile), plus a block table and a bitmap.
+ * If that bf16 staging does not fit the int32 row range, it is dropped and the fp8 path widens
+ * in the kernel, as with the flag.
  * Returns 0 if dims is NULL or invalid. The caller allocates it; contents need no
  * initialisation and may be reused across calls on the same stream. */
 size_t ppa_workspace_bytes(const ppa_dims* dims);

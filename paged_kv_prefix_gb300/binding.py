@@ -26,6 +26,7 @@ PPA_KV_FP8_E4M3 = 1
 PPA_FLAG_CAUSAL = 1
 PPA_FLAG_CLAMP_MM = 2
 PPA_FLAG_NO_PRUNE = 4
+PPA_FLAG_FP8_INKERNEL = 8
 
 
 class PpaDims(ctypes.Structure):

@@ -18,7 +18,8 @@ namespace {
 
 using ppa::WsHeader;
 
-constexpr unsigned kKnownFlags = PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE;
+constexpr unsigned kKnownFlags =
+    PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE | PPA_FLAG_FP8_INKERNEL;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -60,7 +61,12 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
 }
 
 struct WsLayout {
-  size_t header, seq_unit_base, seq_cost, seq_order, seq_item_base, units, items, total;
+  size_t header, seq_unit_base, seq_cost, seq_order, seq_item_base, units, items;
+  // fp8 caches dequantised before the attention kernel (see ppa_fp8_dequant.cu)
+  bool fp8_scratch;
+  int fp8_tiles_per_seq, fp8_words_per_seq;
+  size_t fp8_bits, fp8_table, fp8_k, fp8_v;
+  size_t total;
 };
 
 WsLayout ws_layout(const ppa_dims* d) {
@@ -75,6 +81,25 @@ WsLayout ws_layout(const ppa_dims* d) {
   w.units = align_up(w.seq_item_base + seq_ints * 4, 256);
   w.items = align_up(w.units + (size_t)mq * sizeof(ppa::Unit), 256);
   w.total = align_up(w.items + (size_t)mq * d->num_kv_heads * 4, 256);
+  w.fp8_scratch = false;
+  w.fp8_tiles_per_seq = w.fp8_words_per_seq = 0;
+  w.fp8_bits = w.fp8_table = w.fp8_k = w.fp8_v = w.total;
+  if (d->kv_dtype == PPA_KV_FP8_E4M3 && !(d->flags & PPA_FLAG_FP8_INKERNEL)) {
+    const long long tn = ppa::keys_per_tile(d->head_dim);
+    const long long tiles = ((long long)d->max_pages_per_seq * d->page_size + tn - 1) / tn;
+    const long long pages = tiles * d->num_seqs;
+    if (pages > 0 && pages * tn <= INT_MAX) {  // scratch rows must fit the kernel's int32 rows
+      const size_t row_bytes = (size_t)d->num_kv_heads * d->head_dim * 2;
+      w.fp8_scratch = true;
+      w.fp8_tiles_per_seq = (int)tiles;
+      w.fp8_words_per_seq = (int)((tiles + 31) / 32);
+      w.fp8_bits = w.total;
+      w.fp8_table = align_up(w.fp8_bits + (size_t)d->num_seqs * w.fp8_words_per_seq * 4, 256);
+      w.fp8_k = align_up(w.fp8_table + (size_t)pages * 4, 256);
+      w.fp8_v = align_up(w.fp8_k + (size_t)pages * tn * row_bytes, 256);
+      w.total = align_up(w.fp8_v + (size_t)pages * tn * row_bytes, 256);
+    }
+  }
   return w;
 }
 
@@ -219,29 +244,65 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.num_pages = dims->num_pages;
   a.max_pages_per_seq = dims->max_pages_per_seq;
   const int D = dims->head_dim;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // fp8 with scratch: dequantise the live cache tiles once, then run the bf16 kernel on them,
+  // read as a paged cache of 128-token pages through the identity block table.
+  const bool prepass = fp8 && w.fp8_scratch;
+  if (prepass) {
+    ppa::Fp8DequantParams f{};
+    f.ws = a.ws;
+    f.units = a.units;
+    f.max_units = (int)mq;
+    f.context_lens = context_lens;
+    f.block_table = block_table;
+    f.k_cache = k_cache;
+    f.v_cache = v_cache;
+    f.k_scale = k_scale;
+    f.v_scale = v_scale;
+    f.k_out = ws + w.fp8_k;
+    f.v_out = ws + w.fp8_v;
+    f.table = reinterpret_cast<int32_t*>(ws + w.fp8_table);
+    f.live_bits = reinterpret_cast<uint32_t*>(ws + w.fp8_bits);
+    f.status = device_status;
+    f.num_seqs = dims->num_seqs;
+    f.tiles_per_seq = w.fp8_tiles_per_seq;
+    f.words_per_seq = w.fp8_words_per_seq;
+    f.tn = ppa::keys_per_tile(D);
+    f.page_size = dims->page_size;
+    f.num_pages = dims->num_pages;
+    f.max_pages_per_seq = dims->max_pages_per_seq;
+    f.row_codes = dims->num_kv_heads * D;
+    if (ppa::launch_fp8_dequant(f, s) != cudaSuccess) return PPA_ERR_CUDA;
+    a.k_cache = f.k_out;
+    a.v_cache = f.v_out;
+    a.block_table = f.table;
+    a.page_size = f.tn;
+    a.num_pages = dims->num_seqs * w.fp8_tiles_per_seq;
+    a.max_pages_per_seq = w.fp8_tiles_per_seq;
+  }
+  const bool fp8_kernel = fp8 && !prepass;
   bool maps_ok =
       encode_rows(&a.tm.q, q, D, dims->num_q_heads, dims->total_q, G, tq) &&
       encode_rows(&a.tm.k_new, k_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
       encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
       encode_rows(&a.tm.k_new32, k_new, D, dims->num_kv_heads, dims->total_q, 1, 32) &&
       encode_rows(&a.tm.v_new32, v_new, D, dims->num_kv_heads, dims->total_q, 1, 32);
-  if (maps_ok && !fp8) {
-    const long long cache_rows = (long long)dims->num_pages * dims->page_size;
-    maps_ok = encode_rows(&a.tm.k_cache, k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
-              encode_rows(&a.tm.v_cache, v_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
-              encode_rows(&a.tm.k_cache32, k_cache, D, dims->num_kv_heads, cache_rows, 1, 32) &&
-              encode_rows(&a.tm.v_cache32, v_cache, D, dims->num_kv_heads, cache_rows, 1, 32);
+  if (maps_ok && !fp8_kernel) {
+    const long long cache_rows = (long long)a.num_pages * a.page_size;
+    maps_ok = encode_rows(&a.tm.k_cache, a.k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
+              encode_rows(&a.tm.v_cache, a.v_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
+              encode_rows(&a.tm.k_cache32, a.k_cache, D, dims->num_kv_heads, cache_rows, 1, 32) &&
+              encode_rows(&a.tm.v_cache32, a.v_cache, D, dims->num_kv_heads, cache_rows, 1, 32);
   }
   if (!maps_ok) return PPA_ERR_CUDA;
   const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);
   a.scale_log2 = sm * 1.4426950408889634f;
   const int max_items = (int)(mq * dims->num_kv_heads);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (dims->head_dim) {
-    case 64: e = ppa::launch_attn_d64(a, fp8, max_items, s); break;
-    case 128: e = ppa::launch_attn_d128(a, fp8, max_items, s); break;
-    default: e = ppa::launch_attn_d256(a, fp8, max_items, s); break;
+    case 64: e = ppa::launch_attn_d64(a, fp8_kernel, max_items, s); break;
+    case 128: e = ppa::launch_attn_d128(a, fp8_kernel, max_items, s); break;
+    default: e = ppa::launch_attn_d256(a, fp8_kernel, max_items, s); break;
   }
   return e == cudaSuccess ? PPA_OK : PPA_ERR_CUDA;
 }

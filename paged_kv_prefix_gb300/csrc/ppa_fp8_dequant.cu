@@ -1,0 +1,133 @@
+// fp8 caches: dequantise the live cache key tiles of a batch into bf16 scratch, once per call.
+//
+// Without this pass every unit of work (two query tiles of one sequence and one KV head)
+// widens each e4m3 key tile it visits, so a tile shared by the many units of one long
+// sequence is converted once per unit, by producer warps that compete with the softmax for
+// issue slots. Here each live tile is converted once, by a memory-bound kernel, and the
+// attention kernel then runs its bf16 path on the scratch.
+//
+// Scratch layout: "pages" of TN (=128) tokens, page b * tiles_per_seq + t holding cache
+// positions [t * TN, t * TN + TN) of sequence b, each position [Hkv][D] bf16 like the cache.
+// The identity block table (entry b * tiles_per_seq + t = b * tiles_per_seq + t) goes next
+// to it, so the attention kernel reads the scratch as a paged cache with page size TN whose
+// key tiles never straddle a page. Only tiles some unit visits are written; the attention
+// kernel reads no others (the same live-tile intervals drive both). Rows past the context
+// end of a sequence's last cache tile are not written and not read (the attention kernel
+// takes those keys from the new-token tensors).
+//
+// Each value is bf16(decode(code) * scale), the fp32 product rounded once, as in the
+// in-kernel path when it applies the scales itself.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ppa_internal.cuh"
+#include "ppa_kernels.h"
+#include "ppa_ptx.cuh"
+
+namespace ppa {
+namespace {
+
+// One thread per unit: marks the cache key tiles [lo, min(hi, ceil(c / TN))) of its sequence,
+// a word of 32 tiles per atomic.
+__global__ void fp8_mark_kernel(Fp8DequantParams p) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= p.max_units || u >= p.ws->n_units) return;
+  const Unit un = p.units[u];
+  const int lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
+  int hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
+  const int c = p.context_lens[un.seq];
+  hi = min(hi, (c + p.tn - 1) / p.tn);
+  hi = min(hi, p.tiles_per_seq);
+  uint32_t* bits = p.live_bits + (size_t)un.seq * p.words_per_seq;
+  for (int t = max(lo, 0); t < hi;) {
+    const int w = t >> 5, b0 = t & 31;
+    const int b1 = min(32, b0 + (hi - t));  // bits [b0, b1) of word w
+    const uint32_t m = (b1 - b0 == 32) ? 0xFFFFFFFFu : (((1u << (b1 - b0)) - 1u) << b0);
+    atomicOr(bits + w, m);
+    t += b1 - b0;
+  }
+}
+
+// One CTA per (sequence, key tile) and tensor (blockIdx.y: 0 = K, 1 = V). Writes the identity
+// block-table entry, then, if the tile is live, the bf16 rows of its cache positions.
+constexpr int kDequantThreads = 256;
+
+__global__ void __launch_bounds__(kDequantThreads) fp8_dequant_kernel(Fp8DequantParams p) {
+  const int b = blockIdx.x / p.tiles_per_seq;
+  const int t = blockIdx.x - b * p.tiles_per_seq;
+  const int page = blockIdx.x;  // = b * tiles_per_seq + t
+  if (blockIdx.y == 0 && threadIdx.x == 0) p.table[page] = page;
+  if (!((p.live_bits[(size_t)b * p.words_per_seq + (t >> 5)] >> (t & 31)) & 1u)) return;
+  const bool is_v = blockIdx.y != 0;
+  const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
+  uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_out : p.k_out);
+  const float scale = *(is_v ? p.v_scale : p.k_scale);
+  const int c = p.context_lens[b];
+  const int rows = min(p.tn, c - t * p.tn);  // cache positions in this tile (>= 1: live)
+  const int row_bytes = p.row_codes;         // Hkv * D codes per position
+  const int pieces_per_row = row_bytes / 16;
+  const int pieces = rows * pieces_per_row;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_pages_per_seq;
+  // Four 16-byte pieces in flight per thread before any is widened.
+  constexpr int kUnroll = 4;
+  for (int base = threadIdx.x; base < pieces; base += kDequantThreads * kUnroll) {
+    uint4 codes[kUnroll];
+    int outp[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int i = base + k * kDequantThreads;
+      outp[k] = -1;
+      codes[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < pieces) {
+        const int r = i / pieces_per_row, pc = i - r * pieces_per_row;
+        const int pos = t * p.tn + r;
+        const int lp = pos / p.page_size;
+        const int pg = bt[lp];
+        outp[k] = i;
+        if (pg >= 0 && pg < p.num_pages) {
+          const size_t off =
+              ((size_t)pg * p.page_size + (pos - lp * p.page_size)) * row_bytes + pc * 16;
+          codes[k] = ld_global_nc_v4(src + off);
+        } else {
+          report(p.status, PPA_ERR_BAD_PAGE);  // the row reads as zero, as in the attention
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      if (outp[k] < 0) continue;
+      const uint32_t cw[4] = {codes[k].x, codes[k].y, codes[k].z, codes[k].w};
+      uint32_t v[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        v[2 * q4] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] & 0xFFFFu), scale);
+        v[2 * q4 + 1] = e4m3x2_to_bf16x2_scaled(static_cast<uint16_t>(cw[q4] >> 16), scale);
+      }
+      const int i = outp[k];
+      const int r = i / pieces_per_row, pc = i - r * pieces_per_row;
+      uint4* o = reinterpret_cast<uint4*>(
+          dst + ((size_t)page * p.tn + r) * (size_t)row_bytes * 2 + (size_t)pc * 32);
+      o[0] = make_uint4(v[0], v[1], v[2], v[3]);
+      o[1] = make_uint4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_dequant(const Fp8DequantParams& p, cudaStream_t stream) {
+  const size_t bits_bytes = (size_t)p.num_seqs * p.words_per_seq * sizeof(uint32_t);
+  cudaError_t e = cudaMemsetAsync(p.live_bits, 0, bits_bytes, stream);
+  if (e != cudaSuccess) return e;
+  if (p.max_units > 0) {
+    fp8_mark_kernel<<<(p.max_units + 255) / 256, 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid((unsigned)(p.num_seqs * p.tiles_per_seq), 2u);
+  fp8_dequant_kernel<<<grid, kDequantThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ppa

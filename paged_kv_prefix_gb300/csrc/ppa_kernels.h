@@ -84,6 +84,28 @@ cudaError_t launch_live_kv_tokens(const MaskParams& mp, int num_seqs, const int3
                                   cudaStream_t stream);
 cudaError_t launch_e4m3_decode(const uint8_t* codes, uint16_t* out, int n, cudaStream_t stream);
 
+// fp8 caches: the live cache key tiles of a planned batch, dequantised to bf16 scratch pages of
+// TN tokens (ppa_fp8_dequant.cu).
+struct Fp8DequantParams {
+  const WsHeader* ws;  // the plan's header (n_units)
+  const Unit* units;
+  int max_units;       // capacity of `units`
+  const int32_t* context_lens;
+  const int32_t* block_table;
+  const void* k_cache;  // e4m3 codes [num_pages][page_size][Hkv][D]
+  const void* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  void* k_out;          // bf16 [num_seqs * tiles_per_seq][tn][Hkv][D]
+  void* v_out;
+  int32_t* table;       // identity block table [num_seqs * tiles_per_seq]
+  uint32_t* live_bits;  // [num_seqs][words_per_seq]
+  int32_t* status;
+  int num_seqs, tiles_per_seq, words_per_seq, tn, page_size, num_pages, max_pages_per_seq;
+  int row_codes;  // Hkv * D
+};
+cudaError_t launch_fp8_dequant(const Fp8DequantParams& p, cudaStream_t stream);
+
 // Attention kernels, one translation unit per head dimension. `max_ctas` bounds the
 // persistent grid (the number of work items cannot be known on the host).
 cudaError_t launch_attn_d64(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);

@@ -66,23 +66,49 @@ def test_windows_and_ranges_combined(causal):
                          window_left=70, window_right=33, mm_ranges=mm, clamp_mm=False, seed=8))
 
 
-def test_fp8_kv_scaled():
-    parity(wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=9, scale=1 / 16, num_seqs=4))
+# The two fp8 paths: live cache tiles dequantised into workspace before the attention kernel
+# (the default), or widened by the kernel's producers (PPA_FLAG_FP8_INKERNEL).
+FP8_PATHS = pytest.mark.parametrize("fp8_path", [0, binding.PPA_FLAG_FP8_INKERNEL],
+                                    ids=["prepass", "inkernel"])
 
 
+@FP8_PATHS
+def test_fp8_kv_scaled(fp8_path):
+    parity(wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=9, scale=1 / 16, num_seqs=4),
+           flags_extra=fp8_path)
+
+
+@FP8_PATHS
 @pytest.mark.parametrize("page", [16, 37])
 @pytest.mark.parametrize("windowed", [False, True])
-def test_fp8_kv_head_dim_256(page, windowed):
-    """fp8 cache at head_dim 256: each CTA of the pair widens its half of every K and V row."""
+def test_fp8_kv_head_dim_256(page, windowed, fp8_path):
+    """fp8 cache at head_dim 256 (in the kernel: each CTA of the pair widens its half of every
+    K and V row)."""
     rng = np.random.default_rng(page + 2 * windowed)
     ctx = [0, 45, int(rng.integers(200, 400)), 130]
     qlen = [17, 1, int(rng.integers(150, 300)), 64]
     parity(wl.build_case("fp8_d256", ctx, qlen, 8, 4, 256, page, causal=True,
-                         window_left=100 if windowed else 0, kv_dtype="fp8_e4m3", seed=page))
+                         window_left=100 if windowed else 0, kv_dtype="fp8_e4m3", seed=page),
+           flags_extra=fp8_path)
 
 
+@FP8_PATHS
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("page", [1, 5, 37, 128, 300])
+def test_fp8_ragged_geometry(head_dim, page, fp8_path):
+    """Contexts that end mid-tile, on a tile boundary or are empty; a window that leaves the
+    first cache tiles dead; pages smaller and larger than a key tile."""
+    rng = np.random.default_rng(head_dim + page)
+    ctx = [0, 1, 127, 128, 129, int(rng.integers(300, 700)), 256]
+    qlen = [5, 0, 3, 40, 1, int(rng.integers(100, 260)), 130]
+    parity(wl.build_case("fp8_ragged", ctx, qlen, 6, 2, head_dim, page, causal=True,
+                         window_left=int(rng.choice([0, 150])), kv_dtype="fp8_e4m3", seed=page),
+           flags_extra=fp8_path)
+
+
+@FP8_PATHS
 @pytest.mark.parametrize("head_dim", [128, 256])
-def test_fp8_kv_scales_of_2_8_and_above(head_dim):
+def test_fp8_kv_scales_of_2_8_and_above(head_dim, fp8_path):
     """Dequantisation scales >= 2^8 take the widening's two-multiply branch (scale * 2^120
     would overflow fp32). K's scale grows by 2^16 and the softmax scale shrinks by the same
     power of two, so the logits keep their size; V's outputs grow by 2^16."""
@@ -93,7 +119,7 @@ def test_fp8_kv_scales_of_2_8_and_above(head_dim):
     case = dataclasses.replace(base, k_scale=base.k_scale * big, v_scale=base.v_scale * big,
                                sm_scale=head_dim ** -0.5 / big)
     assert case.k_scale >= 256 and case.v_scale >= 256
-    got = run_gpu(case).out.float().cpu().numpy()
+    got = run_gpu(case, flags_extra=fp8_path).out.float().cpu().numpy()
     want = ref.attention(case.numpy_inputs())
     # the tolerance applies at the outputs' own magnitude: compare both divided by 2^16
     assert_close(got / big, want / big, case.name)

@@ -52,6 +52,17 @@ def test_tiles_and_workspace():
     assert binding.ppa_query_tiles(_dims(head_dim=96)) == (0, 0)
 
 
+def test_fp8_workspace_holds_the_bf16_staging_unless_widened_in_kernel():
+    base = binding.ppa_workspace_bytes(_dims())
+    fp8 = _dims(kv_dtype=binding.PPA_KV_FP8_E4M3)
+    inkernel = _dims(kv_dtype=binding.PPA_KV_FP8_E4M3, flags=fp8.flags | binding.PPA_FLAG_FP8_INKERNEL)
+    assert binding.ppa_workspace_bytes(inkernel) == base
+    # K and V tiles of 128 positions for every block-table slot of every sequence
+    tiles = fp8.num_seqs * -(-(fp8.max_pages_per_seq * fp8.page_size) // 128)
+    staging = 2 * tiles * 128 * fp8.num_kv_heads * fp8.head_dim * 2
+    assert staging <= binding.ppa_workspace_bytes(fp8) - base <= staging + 4 * 256 + 8 * tiles
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 96, binding.PPA_ERR_UNSUPPORTED),
     ("num_kv_heads", 3, binding.PPA_ERR_INVALID),
