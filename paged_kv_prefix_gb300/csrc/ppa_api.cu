@@ -62,6 +62,8 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
 
 struct WsLayout {
   size_t header, seq_unit_base, seq_cost, seq_order, seq_item_base, units, items;
+  size_t row_bounds;  // [total_q][2] row intervals; only with multimodal ranges
+  bool has_row_bounds;
   // fp8 caches dequantised before the attention kernel (see ppa_fp8_dequant.cu)
   bool fp8_scratch;
   int fp8_tiles_per_seq, fp8_words_per_seq;
@@ -81,6 +83,9 @@ WsLayout ws_layout(const ppa_dims* d) {
   w.units = align_up(w.seq_item_base + seq_ints * 4, 256);
   w.items = align_up(w.units + (size_t)mq * sizeof(ppa::Unit), 256);
   w.total = align_up(w.items + (size_t)mq * d->num_kv_heads * 4, 256);
+  w.has_row_bounds = d->max_mm_ranges > 0;
+  w.row_bounds = w.total;
+  if (w.has_row_bounds) w.total = align_up(w.row_bounds + (size_t)d->total_q * 8, 256);
   w.fp8_scratch = false;
   w.fp8_tiles_per_seq = w.fp8_words_per_seq = 0;
   w.fp8_bits = w.fp8_table = w.fp8_k = w.fp8_v = w.total;
@@ -187,9 +192,13 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   s1.items = reinterpret_cast<int32_t*>(ws + w.items);
   s1.bounds_out = nullptr;
   s1.status = device_status;
-  return ppa::launch_plan(s1, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PPA_OK
-             : PPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ppa::launch_plan(s1, s) != cudaSuccess) return PPA_ERR_CUDA;
+  if (w.has_row_bounds &&
+      ppa::launch_row_bounds(s1.mask, dims->num_seqs, dims->total_q, cu_query_lens, context_lens,
+                             reinterpret_cast<int32_t*>(ws + w.row_bounds), s) != cudaSuccess)
+    return PPA_ERR_CUDA;
+  return PPA_OK;
 }
 
 ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
@@ -234,6 +243,7 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.ws = reinterpret_cast<WsHeader*>(ws + w.header);
   a.units = reinterpret_cast<const ppa::Unit*>(ws + w.units);
   a.items = reinterpret_cast<const int32_t*>(ws + w.items);
+  a.row_bounds = w.has_row_bounds ? reinterpret_cast<const int32_t*>(ws + w.row_bounds) : nullptr;
   a.status = device_status;
   a.mask = mask_of(dims, mm_ranges);
   a.num_q_heads = dims->num_q_heads;

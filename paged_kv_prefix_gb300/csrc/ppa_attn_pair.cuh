@@ -444,23 +444,33 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
   const float neg_inf = -__int_as_float(0x7f800000);
   const float scale = p.scale_log2;
   const uint32_t p_full = sh.lead(wsbar::P_FULL), o_empty = sh.lead(wsbar::O_EMPTY);
-  uint32_t od_phase = 0, sc = 0, kv_next = 0;
-  for (int k = 0;; ++k) {
-    const int item = pair_ring_get(sh, k);
-    if (item < 0) break;
-    const UnitInfo u = decode_item(p, item);
-    const uint32_t kv0 = kv_next;
-    kv_next += u.hi - u.lo;
+  uint32_t od_phase = 0, sc = 0;
+  const int tok = r / p.group, hh = r % p.group;
+  // This thread's row of one unit. The next unit's is prepared right after the last P of the
+  // current unit, before its epilogue: the ring's release arrival then has no output stores
+  // to wait for, and the item's dependent loads and the range scan overlap the last PV.
+  struct RowPlan {
+    UnitInfo u;
+    uint32_t kv0;  // K/V ring position of the unit's first key tile
+    int j, kmin, kmax;
+    bool row_valid;
+  };
+  auto plan_row = [&](int item, uint32_t kv0, RowPlan& rp) {
+    rp.u = decode_item(p, item);
+    rp.kv0 = kv0;
+    rp.j = (rp.u.t0 + i) * p.tq + tok;
+    rp.row_valid = i < rp.u.nt && tok < p.tq && rp.j < rp.u.n;
+    row_bounds_of(p, rp.u, rp.j, rp.row_valid, rp.kmin, rp.kmax);
+  };
+  int item = pair_ring_get(sh, 0);
+  RowPlan cur;
+  if (item >= 0) plan_row(item, 0u, cur);
+  for (int k = 0; item >= 0; ++k) {
+    const UnitInfo& u = cur.u;
+    const uint32_t kv0 = cur.kv0;
     const int lo = u.lo, hi = u.hi;  // the pair walks the union of both tiles' intervals
-    const int tok = r / p.group, hh = r % p.group;
-    const int j = (u.t0 + i) * p.tq + tok;
-    const bool row_valid = i < u.nt && tok < p.tq && j < u.n;
-    int kmin = 0, kmax = u.s - 1;  // padding rows attend everywhere (finite values)
-    if (row_valid) {
-      const int32_t* ranges =
-          p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)u.b * p.mask.max_mm_ranges * 2 : nullptr;
-      row_interval(u.c + j, u.s, p.mask, ranges, kmin, kmax);
-    }
+    const int j = cur.j, kmin = cur.kmin, kmax = cur.kmax;
+    const bool row_valid = cur.row_valid;
     float m_ref = neg_inf, l_run = 0.f;
     bool ok = true;
     for (int kt = lo; kt < hi; ++kt) {
@@ -557,6 +567,9 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
       if ((threadIdx.x & 31) == 0) mbar_arrive_cluster_relaxed(p_full);  // P is in TMEM
     }
     if (!ok) break;
+    const int next = pair_ring_get(sh, k + 1);
+    RowPlan nxt = cur;
+    if (next >= 0) plan_row(next, kv0 + static_cast<uint32_t>(hi - lo), nxt);
     // ---- epilogue: the last PV; O / l to bf16 ----
     if (!wait_warp(sh.ws, wsbar::O_DONE, od_phase)) break;
     od_phase ^= 1;
@@ -565,24 +578,37 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
     __nv_bfloat16* orow =
         static_cast<__nv_bfloat16*>(p.out) +
         ((size_t)(u.q_start + (row_valid ? j : 0)) * p.num_q_heads + u.g * p.group + hh) * D;
+    auto store32 = [&](const uint32_t (&o32)[32], int cc) {
+      if (!row_valid) return;
+      uint32_t wv[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        wv[e] = pack_bf16x2(__uint_as_float(o32[2 * e]) * inv_l,
+                            __uint_as_float(o32[2 * e + 1]) * inv_l);
+      uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+    };
+    // 32-column chunks, the load of the next in flight while one is converted and stored
+    static_assert((D / 32) % 2 == 0, "chunk pairs");
+    uint32_t oa[32], ob[32];
+    tmem_ld_32_async(tO, oa);
+    tmem_ld_wait(oa);
 #pragma unroll 1
-    for (int cc = 0; cc < D / 32; ++cc) {
-      uint32_t o32[32];
-      tmem_ld_32(tO + cc * 32, o32);
-      if (row_valid) {
-        uint32_t wv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          wv[e] = pack_bf16x2(__uint_as_float(o32[2 * e]) * inv_l,
-                              __uint_as_float(o32[2 * e + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
-      }
+    for (int cc = 0; cc < D / 32; cc += 2) {
+      tmem_ld_32_async(tO + (cc + 1) * 32, ob);
+      store32(oa, cc);
+      tmem_ld_wait(ob);
+      if (cc + 2 < D / 32) tmem_ld_32_async(tO + (cc + 2) * 32, oa);
+      store32(ob, cc + 1);
+      if (cc + 2 < D / 32) tmem_ld_wait(oa);
     }
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive_cluster_relaxed(o_empty);  // O was read from TMEM
+    item = next;
+    cur = nxt;
   }
 }
 

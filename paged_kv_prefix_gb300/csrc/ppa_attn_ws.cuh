@@ -174,6 +174,23 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   return u;
 }
 
+// The allowed key interval of row j (query position c + j) of unit u: with multimodal ranges
+// it comes from the per-token table the plan stage wrote (one load instead of a scan over
+// every range); otherwise from the closed form. Padding rows (not valid) attend everywhere.
+__device__ __forceinline__ void row_bounds_of(const AttnParams& p, const UnitInfo& u, int j,
+                                              bool valid, int& kmin, int& kmax) {
+  kmin = 0;
+  kmax = u.s - 1;
+  if (!valid) return;
+  if (p.row_bounds != nullptr) {
+    const int2 kb = *reinterpret_cast<const int2*>(p.row_bounds + 2 * (size_t)(u.q_start + j));
+    kmin = kb.x;
+    kmax = kb.y;
+  } else {
+    row_interval(u.c + j, u.s, p.mask, nullptr, kmin, kmax);
+  }
+}
+
 // The same unit in every lane, taken from lane 0, so the compiler can keep it warp-uniform.
 __device__ __forceinline__ UnitInfo uniform_unit(UnitInfo u) {
   int* f = reinterpret_cast<int*>(&u);
@@ -673,12 +690,8 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     const int tok = r / p.group, hh = r % p.group;
     const int j = (u.t0 + i) * p.tq + tok;
     const bool row_valid = tok < p.tq && j < u.n;
-    int kmin = 0, kmax = u.s - 1;  // padding rows attend everywhere (Q is zero: finite)
-    if (row_valid) {
-      const int32_t* ranges =
-          p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)u.b * p.mask.max_mm_ranges * 2 : nullptr;
-      row_interval(u.c + j, u.s, p.mask, ranges, kmin, kmax);
-    }
+    int kmin, kmax;  // padding rows attend everywhere (Q is zero: finite)
+    row_bounds_of(p, u, j, row_valid, kmin, kmax);
     float m_ref = neg_inf, l_run = 0.f;
     bool ok = true;
     for (int kt = lo; kt < hi; ++kt) {

@@ -60,6 +60,7 @@ struct AttnParams {
   WsHeader* ws;
   const Unit* units;
   const int32_t* items;
+  const int32_t* row_bounds;  // [total_q][2] row intervals when multimodal ranges are given
   int32_t* status;
   MaskParams mask;
   int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
@@ -83,6 +84,9 @@ cudaError_t launch_live_kv_tokens(const MaskParams& mp, int num_seqs, const int3
                                   const int32_t* ctx, unsigned long long* out,
                                   cudaStream_t stream);
 cudaError_t launch_e4m3_decode(const uint8_t* codes, uint16_t* out, int n, cudaStream_t stream);
+// Per query token, its row's allowed key interval [kmin, kmax] (out: [total_q][2]).
+cudaError_t launch_row_bounds(const MaskParams& mp, int num_seqs, int total_q, const int32_t* cu,
+                              const int32_t* ctx, int32_t* out, cudaStream_t stream);
 
 // fp8 caches: the live cache key tiles of a planned batch, dequantised to bf16 scratch pages of
 // TN tokens (ppa_fp8_dequant.cu).

@@ -314,6 +314,31 @@ __global__ void live_pairs_kernel(const MaskParams mp, int num_seqs, int total_q
   if ((threadIdx.x & 31) == 0 && acc) atomicAdd(out, acc);
 }
 
+// One thread per query token: the allowed key interval [kmin, kmax] of its row (row_interval),
+// for the attention kernels to load instead of scanning the multimodal ranges once per unit.
+// Sequence lookup by binary search over cu_query_lens, as in live_pairs_kernel; tokens of a
+// sequence whose lengths are invalid get some interval, but the plan then schedules no work.
+__global__ void row_bounds_kernel(const MaskParams mp, int num_seqs, int total_q,
+                                  const int32_t* cu, const int32_t* ctx, int32_t* out) {
+  for (int tok = blockIdx.x * blockDim.x + threadIdx.x; tok < total_q;
+       tok += gridDim.x * blockDim.x) {
+    int lo = 0, hi = num_seqs - 1;  // last sequence with cu[b] <= tok
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int c = ctx[b];
+    const int n = cu[b + 1] - cu[b];
+    const int j = tok - cu[b];
+    const int32_t* ranges = mp.mm_ranges ? mp.mm_ranges + (size_t)b * mp.max_mm_ranges * 2 : nullptr;
+    int kmin = 0, kmax = 0;
+    if (j >= 0 && j < n) row_interval(c + j, c + n, mp, ranges, kmin, kmax);
+    out[2 * (size_t)tok] = kmin;
+    out[2 * (size_t)tok + 1] = kmax;
+  }
+}
+
 // One CTA per sequence: the cached context keys that at least one of its queries may attend
 // to. The union of the rows' allowed intervals is itself an interval (each row's contains the
 // row's own position and the positions are consecutive), so it is [min kmin, max kmax].
@@ -393,6 +418,15 @@ cudaError_t launch_live_kv_tokens(const MaskParams& mp, int num_seqs, const int3
   if (e != cudaSuccess) return e;
   if (num_seqs == 0) return cudaSuccess;
   live_kv_tokens_kernel<<<num_seqs, 256, 0, stream>>>(mp, cu, ctx, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_bounds(const MaskParams& mp, int num_seqs, int total_q, const int32_t* cu,
+                              const int32_t* ctx, int32_t* out, cudaStream_t stream) {
+  if (num_seqs == 0 || total_q == 0) return cudaSuccess;
+  const int blocks = (total_q + 255) / 256;
+  row_bounds_kernel<<<blocks < 4096 ? blocks : 4096, 256, 0, stream>>>(mp, num_seqs, total_q, cu,
+                                                                       ctx, out);
   return cudaGetLastError();
 }
 
