@@ -95,7 +95,9 @@ typedef struct {
   float sm_scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
 } ppa_dims;
 
-/* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list).
+/* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list; with
+ * multimodal ranges (max_mm_ranges > 0) also 8 bytes per query token: each row's allowed key
+ * interval, written by ppa_plan so that the attention kernel does not rescan the ranges).
  * For an fp8 cache without PPA_FLAG_FP8_INKERNEL it also holds the bf16 scratch that the live
  * cache key tiles are dequantised into before the attention kernel runs: room for
  * num_seqs * ceil(max_pages_per_seq * page_size / 128) tiles of 128 positions for K and for
@@ -122,7 +124,8 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
  * a batch (the lengths, ranges and mask parameters do not change between layers).
  *
  * ppa_plan (stage 1): validates the lengths on the device, computes every query tile's
- * live key-tile interval and the work list (heaviest tiles first) into `workspace`.
+ * live key-tile interval and the work list (heaviest tiles first) into `workspace`, and,
+ * with multimodal ranges, every query token's allowed key interval.
  *
  * ppa_attend (stage 2): the attention kernel over the work list in `workspace`. The
  * workspace must hold a plan made by ppa_plan for the same dims and the same
