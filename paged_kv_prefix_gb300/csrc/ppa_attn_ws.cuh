@@ -42,7 +42,7 @@
 
 namespace ppa {
 
-template <int D>
+template <int D, bool FP8 = false>
 struct WsCfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128 (256 runs on CTA pairs)");
   static constexpr int M = kRowsPerTile;  // rows per query tile
@@ -60,10 +60,11 @@ struct WsCfg {
   static constexpr int KV_OFF = Q_OFF + NQ * Q_BYTES;
   static constexpr int STAGE_STRIDE = 2 * KV_BYTES;
   static constexpr int V_OFF = KV_OFF + KV_BYTES;
-  // fp8 caches: per producer warp, a staging area for its 64 rows of raw e4m3 bytes
+  // fp8 caches: per producer warp, a staging area for its 64 rows of raw e4m3 bytes (only
+  // the fp8 instantiation reserves it; every other offset is the same in both)
   static constexpr int STG_OFF = KV_OFF + (NSK + NSV) * KV_BYTES;
   static constexpr int STG_ROWS = TN / 2;  // rows per producer warp
-  static constexpr int STG_BYTES = 4 * STG_ROWS * D;
+  static constexpr int STG_BYTES = FP8 ? 4 * STG_ROWS * D : 0;
   static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = BAR_OFF + BAR_BYTES + 1024;  // + alignment slack
@@ -832,7 +833,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__ AttnParams p) {
-  using C = WsCfg<D>;
+  using C = WsCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -928,7 +929,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
 
 template <int D, bool FP8>
 cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stream) {
-  using C = WsCfg<D>;
+  using C = WsCfg<D, FP8>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
