@@ -37,6 +37,16 @@ Readings where the pages are silent or disagree:
   ``h // (Hq/Hkv)``.
 * fp8 caches hold OCP E4M3 "fn" codes (no infinities, S.1111.111 is NaN). The value is
   ``decode(code) * scale``, with one fp32 scale for K and one for V.
+* KV append (the step before attention in chunked prefill, PR #54194 "功能与动机": the
+  new tokens' K/V land in the paged cache): new token ``j`` of sequence ``b`` is written
+  to position ``c + j`` of the sequence, i.e. page ``block_table[b][(c + j) // P]``, slot
+  ``(c + j) % P``. A bf16 cache takes the value unchanged. An fp8 cache takes the code
+  nearest to ``value / scale`` (the quotient formed in fp32), ties to the even code,
+  magnitudes past 448 saturated to 448, NaN to a NaN code. The pages name only the dtype,
+  so this encoding is a reading: round to nearest even is the IEEE default, and saturation
+  keeps an out-of-range value finite rather than NaN.
+* Cache-sourced attention (``inp["kv_in_cache"]``): the new tokens' K/V are read from the
+  cache at positions ``c .. s-1`` instead of from ``k_new/v_new``.
 """
 from __future__ import annotations
 
@@ -47,6 +57,8 @@ import numpy as np
 
 __all__ = [
     "e4m3fn_table",
+    "e4m3fn_encode",
+    "append_kv",
     "allowed_pair",
     "allowed_mask",
     "gather_kv",
@@ -79,6 +91,26 @@ def e4m3fn_table() -> np.ndarray:
 
 
 _E4M3 = e4m3fn_table()
+
+
+def e4m3fn_encode(x) -> np.ndarray:
+    """Codes of float32 values ``x``: the nearest finite E4M3 value, ties to the even code,
+    magnitudes above the largest finite value (448) saturated to it, NaN to 0x7F. The
+    sign bit is the value's (so -0.0 gives 0x80). Finite positive codes 0x00 .. 0x7E
+    increase with their value, so the search runs over that table."""
+    x = np.asarray(x, dtype=np.float32)
+    mag = np.abs(x).astype(np.float64)
+    pos = _E4M3[:0x7F]  # codes 0 .. 126, ascending, all finite
+    hi = np.clip(np.searchsorted(pos, mag, side="left"), 0, 0x7E)  # first value >= mag
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_hi = np.abs(pos[hi] - mag)
+    d_lo = np.abs(mag - pos[lo])
+    take_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(take_lo, lo, hi)
+    code = np.where(mag >= pos[0x7E], 0x7E, code)  # saturate (also +-inf)
+    code = code | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
 
 
 # ---------------------------------------------------------------------------------------
@@ -156,15 +188,17 @@ def _cache_value(inp: dict, which: str, page: int, slot: int, dtype) -> np.ndarr
 
 
 def gather_kv(inp: dict, b: int, which: str, dtype=np.float32) -> np.ndarray:
-    """K or V of sequence ``b`` at positions ``0 .. s-1``, shape ``[s, Hkv, D]``."""
+    """K or V of sequence ``b`` at positions ``0 .. s-1``, shape ``[s, Hkv, D]``. With
+    ``inp["kv_in_cache"]`` every position comes from the cache."""
     P = inp["page_size"]
     c = int(inp["context_lens"][b])
     cu = inp["cu_query_lens"]
     n = int(cu[b + 1] - cu[b])
     new = inp[f"{which}_new"]
+    from_cache = c + n if inp.get("kv_in_cache") else c
     rows = []
     for p in range(c + n):
-        if p < c:
+        if p < from_cache:
             page = int(inp["block_table"][b, p // P])
             rows.append(_cache_value(inp, which, page, p % P, dtype))
         else:
@@ -233,6 +267,34 @@ def attention(inp: dict, dtype=np.float32, row_chunk: int = 1024) -> np.ndarray:
             toks = np.arange(j0, min(n, j0 + row_chunk))
             out[int(cu[b]) + toks] = attention_rows(inp, b, toks, dtype, kv)
     return out
+
+
+# ---------------------------------------------------------------------------------------
+# KV append.
+# ---------------------------------------------------------------------------------------
+def append_kv(inp: dict) -> tuple:
+    """The caches after writing every new token: ``(k_cache, v_cache)`` copies, float32
+    values for a bf16 cache, uint8 codes for an fp8 one. Slots no new token maps to keep
+    their contents."""
+    P = inp["page_size"]
+    cu = inp["cu_query_lens"]
+    out = []
+    for which in ("k", "v"):
+        cache = inp[f"{which}_cache"].copy()
+        new = inp[f"{which}_new"]
+        scale = np.float32(inp[f"{which}_scale"])
+        for b in range(len(inp["context_lens"])):
+            c = int(inp["context_lens"][b])
+            for j in range(int(cu[b + 1] - cu[b])):
+                pos = c + j
+                page = int(inp["block_table"][b, pos // P])
+                row = new[int(cu[b]) + j].astype(np.float32)  # [Hkv, D]
+                if inp["kv_dtype"] == "bf16":
+                    cache[page, pos % P] = row
+                else:
+                    cache[page, pos % P] = e4m3fn_encode(row / scale)  # fp32 quotient
+        out.append(cache)
+    return tuple(out)
 
 
 # ---------------------------------------------------------------------------------------

@@ -382,3 +382,87 @@ def test_live_pairs_matches_closed_form_for_causal_window():
             q = c + j
             expect += q - max(0, q - 5) + 1
     assert ref.live_pairs(inp) == expect
+
+
+# ---------------------------------------------------------------------------------------
+# e4m3 encoding and KV append (the step before attention: new tokens land in their pages)
+# ---------------------------------------------------------------------------------------
+def test_e4m3_encode_roundtrips_every_finite_code():
+    table = ref.e4m3fn_table()
+    fin = ~np.isnan(table)
+    codes = np.arange(256)[fin].astype(np.uint8)
+    assert np.array_equal(ref.e4m3fn_encode(table[fin].astype(np.float32)), codes)
+
+
+def test_e4m3_encode_matches_the_library_cast_in_range():
+    rng = np.random.default_rng(40)
+    x = np.concatenate([rng.standard_normal(50000) * 50, rng.standard_normal(50000) * 0.01,
+                        rng.uniform(-448, 448, 20000)]).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref.e4m3fn_encode(x), lib)
+
+
+def test_e4m3_encode_ties_go_to_the_even_code():
+    table = ref.e4m3fn_table()
+    for k in range(0, 0x7E):  # midpoint of codes k and k+1 (exact in fp32: 5 significant bits)
+        mid = np.float32((table[k] + table[k + 1]) / 2)
+        assert float(mid) == (table[k] + table[k + 1]) / 2
+        want = k if k % 2 == 0 else k + 1
+        assert ref.e4m3fn_encode(mid) == want, k
+        assert ref.e4m3fn_encode(-mid) == want | 0x80, k
+
+
+def test_e4m3_encode_saturates_and_keeps_signs():
+    enc = ref.e4m3fn_encode(np.array([1e6, -1e6, np.inf, -np.inf, 449.0, 470.0, -0.0, 0.0],
+                                     dtype=np.float32))
+    assert enc.tolist() == [0x7E, 0xFE, 0x7E, 0xFE, 0x7E, 0x7E, 0x80, 0x00]
+    assert ref.e4m3fn_encode(np.float32(np.nan)) & 0x7F == 0x7F
+
+
+def _appended(case):
+    inp = _inp(case)
+    k, v = ref.append_kv(inp)
+    out = dict(inp)
+    out["k_cache"], out["v_cache"], out["kv_in_cache"] = k, v, True
+    return inp, out
+
+
+@pytest.mark.parametrize("page", [1, 5, 16, 37])
+def test_append_then_cache_sourced_gather_equals_the_new_token_tensors(page):
+    case = wl.build_case("t", [0, 13, 40, 7], [9, 0, 21, 30], 4, 2, 16, page, causal=True,
+                         seed=41 + page)
+    inp, app = _appended(case)
+    for b in range(4):
+        for which in ("k", "v"):
+            assert np.array_equal(ref.gather_kv(app, b, which, np.float64),
+                                  ref.gather_kv(inp, b, which, np.float64)), (b, which)
+    assert np.array_equal(ref.attention(app, np.float64), ref.attention(inp, np.float64))
+
+
+def test_append_touches_only_the_new_tokens_slots():
+    case = wl.build_case("t", [3, 20], [6, 11], 4, 2, 16, 8, causal=True, seed=42)
+    inp, app = _appended(case)
+    P, touched = 8, set()
+    for b, (c, n) in enumerate([(3, 6), (20, 11)]):
+        for pos in range(c, c + n):
+            touched.add((int(inp["block_table"][b, pos // P]), pos % P))
+    for page in range(inp["k_cache"].shape[0]):
+        for slot in range(P):
+            same = np.array_equal(app["k_cache"][page, slot], inp["k_cache"][page, slot],
+                                  equal_nan=True)
+            # untouched slots keep their contents; touched ones lose the NaN poison
+            assert same == ((page, slot) not in touched), (page, slot)
+
+
+def test_append_fp8_stores_the_encoded_quotient():
+    case = wl.build_case("t", [17, 4], [12, 25], 4, 2, 16, 16, causal=True,
+                         kv_dtype="fp8_e4m3", seed=43)
+    inp, app = _appended(case)
+    cu = inp["cu_query_lens"]
+    for b, c in enumerate([17, 4]):
+        K = ref.gather_kv(app, b, "k", np.float64)
+        n = int(cu[b + 1] - cu[b])
+        x = inp["k_new"][int(cu[b]):int(cu[b]) + n].astype(np.float32)
+        codes = ref.e4m3fn_encode(x / np.float32(inp["k_scale"]))
+        assert np.array_equal(K[c:], ref.e4m3fn_table()[codes.astype(np.int64)] * inp["k_scale"])
+        assert np.array_equal(K[:c], ref.gather_kv(inp, b, "k", np.float64)[:c])
