@@ -73,9 +73,14 @@ enum {
   PPA_FLAG_CAUSAL = 1u,   /* base mask is causal (k <= q); window_right is then ignored */
   PPA_FLAG_CLAMP_MM = 2u, /* multimodal keys also obey the left window (q - k < window_left) */
   PPA_FLAG_NO_PRUNE = 4u, /* testing: visit every key tile 0 .. ceil(s/TN)-1 and mask them */
-  PPA_FLAG_FP8_INKERNEL = 8u /* fp8 caches: widen e4m3 rows inside the attention kernel instead
-                              * of dequantising the live cache tiles into workspace first; the
-                              * workspace then needs no bf16 scratch (ignored for bf16 caches) */
+  PPA_FLAG_FP8_INKERNEL = 8u, /* fp8 caches: widen e4m3 rows inside the attention kernel
+                               * instead of dequantising the live cache tiles into workspace
+                               * first; the workspace then needs no bf16 scratch (ignored for
+                               * bf16 caches) */
+  PPA_FLAG_KV_IN_CACHE = 16u  /* the new tokens' K/V are already in the cache at positions
+                               * c .. c+n-1 (for instance written by ppa_append_kv): attention
+                               * reads them from there and k_new / v_new are not read (NULL is
+                               * allowed); block-table rows must then cover c + n positions */
 };
 
 typedef struct {
@@ -110,9 +115,9 @@ size_t ppa_workspace_bytes(const ppa_dims* dims);
 
 /* The attention forward pass. Pointers as in the layout table above; k_scale / v_scale are
  * device pointers to one fp32 each (the per-tensor dequantisation scales), required when
- * kv_dtype is PPA_KV_FP8_E4M3 and ignored otherwise. k_new / v_new must be non-NULL (a
- * cache-sourced path without them returns PPA_ERR_UNSUPPORTED). q, k_new, v_new, k_cache,
- * v_cache and out must be 16-byte aligned. Launches two stages on `stream`: ppa_plan (the
+ * kv_dtype is PPA_KV_FP8_E4M3 and ignored otherwise. k_new / v_new must be non-NULL unless
+ * PPA_FLAG_KV_IN_CACHE is set (then they are not read). q, k_new, v_new, k_cache, v_cache
+ * and out must be 16-byte aligned. Launches two stages on `stream`: ppa_plan (the
  * live-tile bounds and work list) and ppa_attend (the persistent attention kernel). */
 ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
                        const void* k_cache, const void* v_cache, const int32_t* block_table,
@@ -141,6 +146,26 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
                       const int32_t* cu_query_lens, const int32_t* context_lens,
                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
                       void* out, void* workspace, int32_t* device_status, void* stream);
+
+/* KV append: writes the new tokens' K/V into the paged cache, where the cache-sourced path
+ * (PPA_FLAG_KV_IN_CACHE; the k=None path of the PR #54194 report, 实现拆解 item 4) reads
+ * them. The pages print no append code; this is its plain reading. New token j of sequence
+ * b (row cu_query_lens[b] + j of k_new / v_new) is written to position
+ * c = context_lens[b] + j of the sequence: page block_table[b][c / page_size], slot
+ * c % page_size, all KV heads. A bf16 cache takes the values unchanged. An fp8 cache takes, per
+ * element, the E4M3 code nearest to value / scale (the quotient in fp32; ties to the even code;
+ * magnitudes past 448 saturate to 448; NaN stays NaN), with k_scale / v_scale device
+ * pointers to one fp32 each. Nothing else in the caches changes.
+ * Host-side errors (NULL or misaligned pointers, invalid dims) return before any launch. On
+ * the device, a sequence with invalid lengths, or whose new positions pass its block-table
+ * row, writes nothing and sets PPA_ERR_INVALID in *device_status; a page id outside
+ * [0, num_pages) skips that token and sets PPA_ERR_BAD_PAGE. k_new, v_new, k_cache and
+ * v_cache must be 16-byte aligned. Launches one kernel on `stream`. */
+ppa_status ppa_append_kv(const ppa_dims* dims, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, const int32_t* block_table,
+                         const int32_t* cu_query_lens, const int32_t* context_lens,
+                         const float* k_scale, const float* v_scale, int32_t* device_status,
+                         void* stream);
 
 /* Size of the scratch ppa_prefill_noalloc keeps in a static device array: 2 MiB. The scratch a
  * batch needs is ppa_workspace_bytes(): about 32 + 4 * num_kv_heads bytes per query tile plus 16

@@ -27,6 +27,7 @@ PPA_FLAG_CAUSAL = 1
 PPA_FLAG_CLAMP_MM = 2
 PPA_FLAG_NO_PRUNE = 4
 PPA_FLAG_FP8_INKERNEL = 8
+PPA_FLAG_KV_IN_CACHE = 16
 
 
 class PpaDims(ctypes.Structure):
@@ -69,6 +70,7 @@ _SIGNATURES = {
                                  _P]),
     "ppa_query_tiles": (None, [_DIMS, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "ppa_tile_bounds": (_I, [_DIMS, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "ppa_append_kv": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ppa_debug_mask": (_I, [_DIMS, _I, _P, _P, _P, _P, _I, _I, _P]),
     "ppa_live_pairs": (_I, [_DIMS, _P, _P, _P, _P, _P]),
     "ppa_live_kv_tokens": (_I, [_DIMS, _P, _P, _P, _P, _P]),
@@ -189,6 +191,18 @@ def ppa_attend(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table, cu
     return code
 
 
+def ppa_append_kv(dims: PpaDims, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
+                  context_lens, k_scale, v_scale, device_status, stream=None,
+                  check: bool = True) -> int:
+    code = lib().ppa_append_kv(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_table), _ptr(cu_query_lens),
+                               _ptr(context_lens), _ptr(k_scale), _ptr(v_scale),
+                               _ptr(device_status), _stream(stream))
+    if check:
+        _check(code, "ppa_append_kv")
+    return code
+
+
 def ppa_tile_bounds(dims: PpaDims, tq: int, tn: int, cu_query_lens, context_lens, mm_ranges,
                     bounds_out, device_status, stream=None, check: bool = True) -> int:
     code = lib().ppa_tile_bounds(ctypes.byref(dims), tq, tn, _ptr(cu_query_lens),
@@ -286,8 +300,22 @@ class DeviceCase:
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    def _new_kv(self):
+        """k_new / v_new for the attention calls: NULL when the dims say the new tokens' K/V
+        are read from the cache."""
+        if self.dims.flags & PPA_FLAG_KV_IN_CACHE:
+            return None, None
+        return self.k_new, self.v_new
+
+    def append(self, stream=None):
+        """Writes the new tokens' K/V into the cache (ppa_append_kv)."""
+        return ppa_append_kv(self.dims, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                             self.block_table, self.cu_query_lens, self.context_lens,
+                             self.k_scale, self.v_scale, self.status, stream)
+
     def run(self, stream=None, out=None):
-        return ppa_prefill(self.dims, self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+        k_new, v_new = self._new_kv()
+        return ppa_prefill(self.dims, self.q, k_new, v_new, self.k_cache, self.v_cache,
                            self.block_table, self.cu_query_lens, self.context_lens,
                            self.mm_ranges, self.k_scale, self.v_scale,
                            self.out if out is None else out, self.workspace, self.status, stream)
@@ -297,7 +325,8 @@ class DeviceCase:
                         self.workspace, self.status, stream)
 
     def attend(self, stream=None, out=None):
-        return ppa_attend(self.dims, self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+        k_new, v_new = self._new_kv()
+        return ppa_attend(self.dims, self.q, k_new, v_new, self.k_cache, self.v_cache,
                           self.block_table, self.cu_query_lens, self.context_lens,
                           self.mm_ranges, self.k_scale, self.v_scale,
                           self.out if out is None else out, self.workspace, self.status, stream)

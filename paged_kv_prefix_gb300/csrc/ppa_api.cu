@@ -18,8 +18,10 @@ namespace {
 
 using ppa::WsHeader;
 
-constexpr unsigned kKnownFlags =
-    PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE | PPA_FLAG_FP8_INKERNEL;
+constexpr unsigned kKnownFlags = PPA_FLAG_CAUSAL | PPA_FLAG_CLAMP_MM | PPA_FLAG_NO_PRUNE |
+                                 PPA_FLAG_FP8_INKERNEL | PPA_FLAG_KV_IN_CACHE;
+
+bool kv_in_cache(const ppa_dims* d) { return (d->flags & PPA_FLAG_KV_IN_CACHE) != 0u; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -178,6 +180,7 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   s1.page_size = dims->page_size;
   s1.max_pages_per_seq = dims->max_pages_per_seq;
   s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
+  s1.kv_in_cache = kv_in_cache(dims) ? 1 : 0;
   s1.max_qtiles = (int)mq;
   s1.nq = ppa::tiles_per_unit(dims->head_dim);
   s1.mask = mask_of(dims, mm_ranges);
@@ -208,7 +211,8 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
                       void* out, void* workspace, int32_t* device_status, void* stream) {
   const ppa_status st = check_dims(dims);
   if (st != PPA_OK) return st;
-  if (k_new == nullptr || v_new == nullptr) return PPA_ERR_UNSUPPORTED;
+  const bool in_cache = kv_in_cache(dims);
+  if (!in_cache && (k_new == nullptr || v_new == nullptr)) return PPA_ERR_UNSUPPORTED;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       cu_query_lens == nullptr || context_lens == nullptr || out == nullptr ||
       workspace == nullptr || device_status == nullptr)
@@ -216,9 +220,10 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   if (dims->max_mm_ranges > 0 && mm_ranges == nullptr) return PPA_ERR_INVALID;
   const bool fp8 = dims->kv_dtype == PPA_KV_FP8_E4M3;
   if (fp8 && (k_scale == nullptr || v_scale == nullptr)) return PPA_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace))
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
     return PPA_ERR_INVALID;
+  if (!in_cache && (!aligned16(k_new) || !aligned16(v_new))) return PPA_ERR_INVALID;
   if (dims->num_seqs == 0 || dims->total_q == 0) return PPA_OK;  // nothing to compute
 
   const int G = group_of(dims);
@@ -245,6 +250,7 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.items = reinterpret_cast<const int32_t*>(ws + w.items);
   a.row_bounds = w.has_row_bounds ? reinterpret_cast<const int32_t*>(ws + w.row_bounds) : nullptr;
   a.status = device_status;
+  a.kv_in_cache = in_cache ? 1 : 0;
   a.mask = mask_of(dims, mm_ranges);
   a.num_q_heads = dims->num_q_heads;
   a.num_kv_heads = dims->num_kv_heads;
@@ -274,6 +280,8 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
     f.table = reinterpret_cast<int32_t*>(ws + w.fp8_table);
     f.live_bits = reinterpret_cast<uint32_t*>(ws + w.fp8_bits);
     f.status = device_status;
+    f.cu_query_lens = cu_query_lens;
+    f.kv_in_cache = in_cache ? 1 : 0;
     f.num_seqs = dims->num_seqs;
     f.tiles_per_seq = w.fp8_tiles_per_seq;
     f.words_per_seq = w.fp8_words_per_seq;
@@ -291,12 +299,12 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
     a.max_pages_per_seq = w.fp8_tiles_per_seq;
   }
   const bool fp8_kernel = fp8 && !prepass;
-  bool maps_ok =
-      encode_rows(&a.tm.q, q, D, dims->num_q_heads, dims->total_q, G, tq) &&
-      encode_rows(&a.tm.k_new, k_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
-      encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
-      encode_rows(&a.tm.k_new32, k_new, D, dims->num_kv_heads, dims->total_q, 1, 32) &&
-      encode_rows(&a.tm.v_new32, v_new, D, dims->num_kv_heads, dims->total_q, 1, 32);
+  bool maps_ok = encode_rows(&a.tm.q, q, D, dims->num_q_heads, dims->total_q, G, tq);
+  if (maps_ok && !in_cache)  // cache-sourced: the kernel never reads k_new / v_new
+    maps_ok = encode_rows(&a.tm.k_new, k_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
+              encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
+              encode_rows(&a.tm.k_new32, k_new, D, dims->num_kv_heads, dims->total_q, 1, 32) &&
+              encode_rows(&a.tm.v_new32, v_new, D, dims->num_kv_heads, dims->total_q, 1, 32);
   if (maps_ok && !fp8_kernel) {
     const long long cache_rows = (long long)a.num_pages * a.page_size;
     maps_ok = encode_rows(&a.tm.k_cache, a.k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&
@@ -325,21 +333,61 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
   // Validate everything ppa_attend checks before ppa_plan launches anything.
   const ppa_status st = check_dims(dims);
   if (st != PPA_OK) return st;
-  if (k_new == nullptr || v_new == nullptr) return PPA_ERR_UNSUPPORTED;
+  const bool in_cache = kv_in_cache(dims);
+  if (!in_cache && (k_new == nullptr || v_new == nullptr)) return PPA_ERR_UNSUPPORTED;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       out == nullptr)
     return PPA_ERR_INVALID;
   if (dims->kv_dtype == PPA_KV_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr))
     return PPA_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PPA_ERR_INVALID;
+  if (!in_cache && (!aligned16(k_new) || !aligned16(v_new))) return PPA_ERR_INVALID;
   const ppa_status sp = ppa_plan(dims, cu_query_lens, context_lens, mm_ranges, workspace,
                                  device_status, stream);
   if (sp != PPA_OK) return sp;
   return ppa_attend(dims, q, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
                     context_lens, mm_ranges, k_scale, v_scale, out, workspace, device_status,
                     stream);
+}
+
+ppa_status ppa_append_kv(const ppa_dims* dims, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, const int32_t* block_table,
+                         const int32_t* cu_query_lens, const int32_t* context_lens,
+                         const float* k_scale, const float* v_scale, int32_t* device_status,
+                         void* stream) {
+  const ppa_status st = check_dims(dims);
+  if (st != PPA_OK) return st;
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      block_table == nullptr || cu_query_lens == nullptr || context_lens == nullptr ||
+      device_status == nullptr)
+    return PPA_ERR_INVALID;
+  const bool fp8 = dims->kv_dtype == PPA_KV_FP8_E4M3;
+  if (fp8 && (k_scale == nullptr || v_scale == nullptr)) return PPA_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PPA_ERR_INVALID;
+  if (dims->num_seqs == 0 || dims->total_q == 0) return PPA_OK;  // nothing to write
+  ppa::AppendParams a{};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.cu_query_lens = cu_query_lens;
+  a.context_lens = context_lens;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.status = device_status;
+  a.num_seqs = dims->num_seqs;
+  a.total_q = dims->total_q;
+  a.row_elems = dims->num_kv_heads * dims->head_dim;
+  a.page_size = dims->page_size;
+  a.num_pages = dims->num_pages;
+  a.max_pages_per_seq = dims->max_pages_per_seq;
+  a.fp8 = fp8 ? 1 : 0;
+  return ppa::launch_append_kv(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PPA_OK
+             : PPA_ERR_CUDA;
 }
 
 ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* cu_query_lens,
@@ -361,6 +409,7 @@ ppa_status ppa_tile_bounds(const ppa_dims* dims, int tq, int tn, const int32_t* 
   s1.page_size = dims->page_size;
   s1.max_pages_per_seq = dims->max_pages_per_seq;
   s1.no_prune = (dims->flags & PPA_FLAG_NO_PRUNE) ? 1 : 0;
+  s1.kv_in_cache = kv_in_cache(dims) ? 1 : 0;
   const long long mq = max_qtiles_for(dims, tq);
   if (mq > INT_MAX / 2) return PPA_ERR_INVALID;
   s1.max_qtiles = (int)mq;

@@ -171,8 +171,10 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
   const char* g_cache = static_cast<const char*>(w == 0 ? p.k_cache : p.v_cache);
   const char* g_new = static_cast<const char*>(w == 0 ? p.k_new : p.v_new);
   if (lane == 0) {
-    tma_prefetch_desc(tm_new);
-    tma_prefetch_desc(tm_new32);
+    if (!p.kv_in_cache) {  // the new-token maps are encoded only when k_new / v_new are read
+      tma_prefetch_desc(tm_new);
+      tma_prefetch_desc(tm_new32);
+    }
     if constexpr (!FP8) {
       tma_prefetch_desc(tm_cache);
       tma_prefetch_desc(tm_cache32);
@@ -201,10 +203,12 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
       int ctype = 0, crow = 0;  // 1 = cache box, 2 = new-token box, 0 = row gather
       if (lane * 16 < rpw) {
         const int p0 = key0 + half * rpw + 16 * lane;
-        if (p0 >= u.c) {
-          ctype = 2;
-          crow = u.q_start + p0 - u.c;
-        } else if (!FP8 && p0 + 15 < u.c) {
+        if (p0 >= u.cs) {
+          if (!p.kv_in_cache) {  // new tokens (cache-sourced: past the sequence, zero fill)
+            ctype = 2;
+            crow = u.q_start + p0 - u.c;
+          }
+        } else if (!FP8 && p0 + 15 < u.cs) {
           const int lp = p0 / p.page_size;
           if ((p0 + 15) / p.page_size == lp) {
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -252,7 +256,7 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
         if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
           const char* mine = nullptr;
           const int pos = p_row0 + lane;
-          if (pos < u.c) {
+          if (pos < u.cs) {
             const int lp = pos / p.page_size;
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
             if (page >= 0 && page < p.num_pages) {
@@ -267,13 +271,13 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
           }
           if constexpr (FP8) {
             if (w == 0)
-              gather_rows_fp8<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0,
+              gather_rows_fp8<D>(g_cache, row0, fb_mask, u.cs - p_row0,
                                  mine, sX, rows, kv_scale);
             else
-              gather_rows_fp8<C::DH>(static_cast<const char*>(p.k_new), row0, fb_mask,
-                                     u.c - p_row0, mine, sX, rows, kv_scale);
+              gather_rows_fp8<C::DH>(g_cache, row0, fb_mask,
+                                     u.cs - p_row0, mine, sX, rows, kv_scale);
           } else {
-            pair_gather_rows(static_cast<const char*>(p.k_new), row0, fb_mask, mine, sX, rows,
+            pair_gather_rows(g_cache, row0, fb_mask, mine, sX, rows,
                              ncol_blocks * 64);
           }
           any_fallback = true;

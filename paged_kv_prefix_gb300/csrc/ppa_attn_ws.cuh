@@ -151,6 +151,7 @@ __device__ __forceinline__ void ring_put(const WsShared& sh, const AttnParams& p
 
 struct UnitInfo {
   int b, g, t0, nt, c, n, s, q_start, lo, hi;
+  int cs;  // key positions below cs come from the cache: c, or s when K/V are in the cache
   int lo_i[2], hi_i[2];
 };
 
@@ -166,6 +167,7 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   u.q_start = p.cu_query_lens[u.b];
   u.n = p.cu_query_lens[u.b + 1] - u.q_start;
   u.s = u.c + u.n;
+  u.cs = p.kv_in_cache ? u.s : u.c;
   u.lo_i[0] = un.lo0;
   u.hi_i[0] = un.hi0;
   u.lo_i[1] = un.nt > 1 ? un.lo1 : 0;
@@ -351,7 +353,7 @@ __device__ __forceinline__ void gather_rows(const AttnParams& p, int row0, int n
         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(mine), lr & 31));
     if (lr < nrows && ((rowmask >> lr) & 1u))
       cp_async_16(sX + swz128(row0 + lr, ch, C::TN),
-                  rp ? rp + ch * 16 : static_cast<const char*>(p.k_new), rp ? 16u : 0u);
+                  rp ? rp + ch * 16 : static_cast<const char*>(p.k_cache), rp ? 16u : 0u);
   }
 }
 
@@ -373,8 +375,10 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const char* g_cache = static_cast<const char*>(w == 0 ? p.k_cache : p.v_cache);
   const char* g_new = static_cast<const char*>(w == 0 ? p.k_new : p.v_new);
   if (lane == 0) {
-    tma_prefetch_desc(tm_new);
-    tma_prefetch_desc(tm_new32);
+    if (!p.kv_in_cache) {  // the new-token maps are encoded only when k_new / v_new are read
+      tma_prefetch_desc(tm_new);
+      tma_prefetch_desc(tm_new32);
+    }
     if constexpr (!FP8) {
       tma_prefetch_desc(tm_cache);
       tma_prefetch_desc(tm_cache32);
@@ -401,10 +405,12 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       int ctype = 0, crow = 0;  // 1 = cache box, 2 = new-token box, 0 = row gather
       if (lane * 16 < RPW) {
         const int p0 = kt * C::TN + half * RPW + 16 * lane;
-        if (p0 >= u.c) {
-          ctype = 2;
-          crow = u.q_start + p0 - u.c;
-        } else if (!FP8 && p0 + 15 < u.c) {
+        if (p0 >= u.cs) {
+          if (!p.kv_in_cache) {  // new tokens (cache-sourced: past the sequence, zero fill)
+            ctype = 2;
+            crow = u.q_start + p0 - u.c;
+          }
+        } else if (!FP8 && p0 + 15 < u.cs) {
           const int lp = p0 / p.page_size;
           if ((p0 + 15) / p.page_size == lp) {
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -460,7 +466,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
         if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
           const char* mine = nullptr;
           const int pos = p_row0 + lane;
-          if (pos < u.c) {
+          if (pos < u.cs) {
             const int lp = pos / p.page_size;
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
             if (page >= 0 && page < p.num_pages) {
@@ -474,10 +480,10 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
             mine = g_new + ((size_t)(u.q_start + pos - u.c) * p.num_kv_heads + u.g) * D * 2;
           }
           if constexpr (FP8) {
-            fp8_stage_issue<D>(static_cast<const char*>(p.k_new), row0, fb_mask, u.c - p_row0, mine,
+            fp8_stage_issue<D>(g_cache, row0, fb_mask, u.cs - p_row0, mine,
                                sX, C::TN, stg + (32 * sub + lane) * D);
             fp8_mask[sub] = fb_mask;
-            fp8_cache_rows[sub] = u.c - p_row0;
+            fp8_cache_rows[sub] = u.cs - p_row0;
           } else {
             gather_rows<D>(p, row0, 32, fb_mask, mine, sX);
           }
@@ -492,7 +498,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
         for (int sub = 0; sub < NSUB; ++sub) {
           if (sub == 0) cp_async_wait<1>(); else cp_async_wait<0>();
           if (fp8_mask[sub] != 0) {
-            if (kv_fold && u.c >= (kt + 1) * C::TN)  // a cache-only tile: the softmax scales
+            if (kv_fold && u.cs >= (kt + 1) * C::TN)  // a cache-only tile: the softmax scales
               fp8_stage_widen<D, true>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub],
                                        sX, C::TN, stg + (32 * sub + lane) * D, kv_scale);
             else
@@ -724,7 +730,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
       // The constants come from shared memory each tile (no registers held across tiles).
       float2 fc = make_float2(0.f, 0.f);  // (scale_log2 * k_scale * 2^112, log2(v_scale * 2^112))
       if constexpr (FP8) fc = ld_shared_f2(sh.bar(wsbar::FOLD));
-      const bool cache_tile = FP8 && fc.x != 0.f && u.c - k0 >= C::TN;
+      const bool cache_tile = FP8 && fc.x != 0.f && u.cs - k0 >= C::TN;
       const float sc = cache_tile ? fc.x : scale;  // exp2 multiplier
       const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
       if (!(a0 <= 0 && a1 >= C::TN - 1)) {

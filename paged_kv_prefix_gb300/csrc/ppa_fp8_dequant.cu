@@ -11,9 +11,10 @@
 // The identity block table (entry b * tiles_per_seq + t = b * tiles_per_seq + t) goes next
 // to it, so the attention kernel reads the scratch as a paged cache with page size TN whose
 // key tiles never straddle a page. Only tiles some unit visits are written; the attention
-// kernel reads no others (the same live-tile intervals drive both). Rows past the context
-// end of a sequence's last cache tile are not written and not read (the attention kernel
-// takes those keys from the new-token tensors).
+// kernel reads no others (the same live-tile intervals drive both). Rows past a sequence's
+// cache positions (its context, or its context and new tokens when those were appended
+// first) are not written and not read: the attention kernel takes those keys from the
+// new-token tensors, or zero-fills positions past the sequence.
 //
 // Each value is bf16(decode(code) * scale), the fp32 product rounded once, as in the
 // in-kernel path when it applies the scales itself.
@@ -28,16 +29,23 @@
 namespace ppa {
 namespace {
 
-// One thread per unit: marks the cache key tiles [lo, min(hi, ceil(c / TN))) of its sequence,
-// a word of 32 tiles per atomic.
+// Positions of sequence b that are read from the cache: its context, and its new tokens too
+// when they were appended to the cache before the call.
+__device__ __forceinline__ int cache_positions(const Fp8DequantParams& p, int b) {
+  const int c = p.context_lens[b];
+  return p.kv_in_cache ? c + (p.cu_query_lens[b + 1] - p.cu_query_lens[b]) : c;
+}
+
+// One thread per unit: marks the cache key tiles [lo, min(hi, ceil(cs / TN))) of its sequence
+// (cs: its cache positions), a word of 32 tiles per atomic.
 __global__ void fp8_mark_kernel(Fp8DequantParams p) {
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= p.max_units || u >= p.ws->n_units) return;
   const Unit un = p.units[u];
   const int lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
   int hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
-  const int c = p.context_lens[un.seq];
-  hi = min(hi, (c + p.tn - 1) / p.tn);
+  const int cs = cache_positions(p, un.seq);
+  hi = min(hi, (cs + p.tn - 1) / p.tn);
   hi = min(hi, p.tiles_per_seq);
   uint32_t* bits = p.live_bits + (size_t)un.seq * p.words_per_seq;
   for (int t = max(lo, 0); t < hi;) {
@@ -63,8 +71,7 @@ __global__ void __launch_bounds__(kDequantThreads) fp8_dequant_kernel(Fp8Dequant
   const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
   uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_out : p.k_out);
   const float scale = *(is_v ? p.v_scale : p.k_scale);
-  const int c = p.context_lens[b];
-  const int rows = min(p.tn, c - t * p.tn);  // cache positions in this tile (>= 1: live)
+  const int rows = min(p.tn, cache_positions(p, b) - t * p.tn);  // >= 1: the tile is live
   const int row_bytes = p.row_codes;         // Hkv * D codes per position
   const int pieces_per_row = row_bytes / 16;
   const int pieces = rows * pieces_per_row;

@@ -13,6 +13,7 @@ namespace ppa {
 
 struct Stage1Params {
   int num_seqs, total_q, tq, tn, num_kv_heads, page_size, max_pages_per_seq, no_prune;
+  int kv_in_cache;      // block-table rows must cover c + n positions, not c
   int max_qtiles;       // bound on sum_b ceil(n_b / tq); also bounds the number of units
   int nq;               // query tiles per unit (plan mode)
   MaskParams mask;
@@ -62,6 +63,7 @@ struct AttnParams {
   const int32_t* items;
   const int32_t* row_bounds;  // [total_q][2] row intervals when multimodal ranges are given
   int32_t* status;
+  int kv_in_cache;  // new tokens' K/V read from the cache (positions c .. s-1); k_new unused
   MaskParams mask;
   int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
   float scale_log2;  // softmax scale * log2(e)
@@ -105,10 +107,29 @@ struct Fp8DequantParams {
   int32_t* table;       // identity block table [num_seqs * tiles_per_seq]
   uint32_t* live_bits;  // [num_seqs][words_per_seq]
   int32_t* status;
+  const int32_t* cu_query_lens;
+  int kv_in_cache;  // cache positions run to c + n (new tokens already appended), not c
   int num_seqs, tiles_per_seq, words_per_seq, tn, page_size, num_pages, max_pages_per_seq;
   int row_codes;  // Hkv * D
 };
 cudaError_t launch_fp8_dequant(const Fp8DequantParams& p, cudaStream_t stream);
+
+// KV append (ppa_append.cu): new token j of sequence b to cache position c_b + j.
+struct AppendParams {
+  const void* k_new;  // bf16 [total_q][Hkv][D]
+  const void* v_new;
+  void* k_cache;      // bf16 or e4m3 codes [num_pages][page_size][Hkv][D]
+  void* v_cache;
+  const int32_t* block_table;
+  const int32_t* cu_query_lens;
+  const int32_t* context_lens;
+  const float* k_scale;  // fp8 only
+  const float* v_scale;
+  int32_t* status;
+  int num_seqs, total_q, row_elems /* Hkv * D */, page_size, num_pages, max_pages_per_seq;
+  int fp8;
+};
+cudaError_t launch_append_kv(const AppendParams& p, cudaStream_t stream);
 
 // Attention kernels, one translation unit per head dimension. `max_ctas` bounds the
 // persistent grid (the number of work items cannot be known on the host).

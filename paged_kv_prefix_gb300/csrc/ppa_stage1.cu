@@ -59,7 +59,10 @@ __device__ __forceinline__ int seq_query_len(const Stage1Params& p, int b, int* 
   bool ok = (n >= 0) && (c >= 0) && (q0 >= 0) && (c <= INT_MAX - n);
   if (b == 0 && q0 != 0) ok = false;
   if (b == p.num_seqs - 1 && q1 != p.total_q) ok = false;
-  if (ok && c > 0 && (c - 1) / p.page_size >= p.max_pages_per_seq) ok = false;
+  // the block-table row covers every cache position read: c of them, or c + n when the new
+  // tokens' K/V are read from the cache too
+  const int span = p.kv_in_cache ? c + n : c;
+  if (ok && span > 0 && (span - 1) / p.page_size >= p.max_pages_per_seq) ok = false;
   *c_out = c;
   if (!ok) *bad = true;
   return ok ? n : 0;
