@@ -1,7 +1,7 @@
 """Benchmark: chunked-prefill attention over a paged KV cache on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nonpow2|swa64|swa1024|mm|mixed] [--no-cpu-baseline]
+                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached] [--no-cpu-baseline]
                     [--sweep windows]
 
 A step is one pass of the whole hot path over one batch: for every shape of the workload,
@@ -62,6 +62,11 @@ def make_workload(name: str, seed: int):
         return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
                 "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
                 [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
+    if name == "mixed_cached":
+        return ("mixed serving, new tokens appended to the paged cache then attended from it "
+                "(ppa_append_kv + cache-sourced attention): 32 seqs, ctx U[4096,32768], "
+                "q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544, bf16 KV",
+                [wl.mixed(544, False, seed=seed)])
     if name == "mixed_window":
         return ("mixed serving with window_left 4096: 32 seqs, ctx U[4096,32768], q U[512,4096], "
                 "32 q / 4 kv heads, D 128, causal, page 2048, bf16 KV",
@@ -79,10 +84,28 @@ def _prepass(dc) -> bool:
             and not (dc.dims.flags & binding.PPA_FLAG_FP8_INKERNEL))
 
 
+def _kv_in_cache(dc) -> bool:
+    """The step appends the new tokens to the cache and attends from it."""
+    from paged_kv_prefix_gb300 import binding
+    return bool(dc.dims.flags & binding.PPA_FLAG_KV_IN_CACHE)
+
+
 def _launches_per_step(dc) -> int:
     """Kernels of this library per step: the plan and the attention kernel, plus the fp8
-    live-tile marking and dequantisation kernels."""
-    return 2 + (2 if _prepass(dc) else 0)
+    live-tile marking and dequantisation kernels, plus the KV append."""
+    return 2 + (2 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
+
+
+def workload_flags(name: str) -> int:
+    from paged_kv_prefix_gb300 import binding
+    return binding.PPA_FLAG_KV_IN_CACHE if name == "mixed_cached" else 0
+
+
+def append_bytes(case) -> float:
+    """The KV append's algorithmic bytes: every new token's K and V row read (bf16) and
+    written (bf16 or one byte per fp8 code)."""
+    per = 2 + (1 if case.kv_dtype == "fp8_e4m3" else 2)
+    return 2.0 * case.total_q * case.num_kv_heads * case.head_dim * per
 
 
 def load_peaks():
@@ -344,7 +367,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     binding.lib()
     desc, cases = make_workload(args.workload, seed=rank)
-    dcs = [binding.DeviceCase(c, device=dev) for c in cases]
+    dcs = [binding.DeviceCase(c, device=dev, flags_extra=workload_flags(args.workload))
+           for c in cases]
     stream = torch.cuda.current_stream(dev)
 
     # live pairs and FLOPs, live cache tokens and algorithmic bytes, from the library's own
@@ -361,12 +385,16 @@ def run_ours(args):
     def step(ev_list):
         for i, dc in enumerate(dcs):
             ev_list[i][0].record(stream)
+            if _kv_in_cache(dc):
+                dc.append(stream)
+            ev_list[i][3].record(stream)
             dc.plan(stream)
             ev_list[i][1].record(stream)
             dc.attend(stream)
             ev_list[i][2].record(stream)
 
-    mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in dcs]
+    # per shape: step start, after the plan, after the attention, after the append
+    mk = lambda: [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in dcs]
     # clocks: the sampler runs from before the warm-up; samples inside the timed region count
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -401,8 +429,10 @@ def run_ours(args):
     step_ms = [sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(len(dcs))) for ev in events]
     attend_ms = np.array([[ev[i][1].elapsed_time(ev[i][2]) for i in range(len(dcs))]
                           for ev in events])  # [steps, shapes]
-    plan_ms = np.array([[ev[i][0].elapsed_time(ev[i][1]) for i in range(len(dcs))]
+    plan_ms = np.array([[ev[i][3].elapsed_time(ev[i][1]) for i in range(len(dcs))]
                         for ev in events])
+    app_ms = np.array([[ev[i][0].elapsed_time(ev[i][3]) for i in range(len(dcs))]
+                       for ev in events])
     total_ms = max_over_ranks(dist, float(sum(step_ms)), dev)
     all_flops = sum_over_ranks(dist, step_flops * args.steps, dev)
     all_tokens = sum_over_ranks(dist, float(tokens * args.steps), dev)
@@ -440,6 +470,13 @@ def run_ours(args):
                        "gbs": round(nbytes[i] / (a * 1e-3) / 1e9, 1),
                        "live_tflop": round(flops[i] / 1e12, 4),
                        "algorithmic_mb": round(nbytes[i] / 1e6, 2)})
+        if _kv_in_cache(dcs[i]):  # the append kernel against the HBM roofline
+            am = float(app_ms[:, i].mean())
+            gbs = append_bytes(case) / (am * 1e-3) / 1e9
+            shapes[-1]["append"] = {"kernel": "append_kv_kernel", "ms": round(am, 4),
+                                    "algorithmic_mb": round(append_bytes(case) / 1e6, 2),
+                                    "gbs": round(gbs, 1), "peak": float(peaks["hbm_gbs"]),
+                                    "frac": round(gbs / float(peaks["hbm_gbs"]), 4)}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         f, s, sample = oracle_sample(cases, args.cpu_seconds)
@@ -505,6 +542,8 @@ def run_e2e(args, cases, dcs, step_flops, stream, dev):
                 dc.mm_ranges.copy_(hs["mm_ranges"], non_blocking=True)
             dc.k_scale.copy_(hs["k_scale"], non_blocking=True)
             dc.v_scale.copy_(hs["v_scale"], non_blocking=True)
+            if _kv_in_cache(dc):
+                dc.append(stream)
             dc.run(stream)
             hs["out"].copy_(dc.out, non_blocking=True)
 
