@@ -33,13 +33,21 @@ Readings where the pages are silent or disagree:
   end is clipped to ``s - 1``. A query ``q`` inside the range may attend to every key
   inside it (bidirectional). With the clamp flag and a left window, such a key must also
   satisfy ``q - k < W``.
+* Chunked-local attention (``chunk_size > 0``, PR #53147 "关键源码片段", the
+  ``CHUNK_LOOKBACK >= 0`` branch of ``compute_tile_loop_bounds``): the base mask's left
+  edge becomes ``k >= ((q // CS) - LB) * CS`` in place of the left window; the right edge is
+  unchanged. Multimodal ranges are still clamped by the ordinary left window (section
+  "评论区精华": the MM mask is OR-ed on and clamped by the sliding window, so it can re-enable
+  keys before the chunk boundary). The page prints only the tile bound, taken at the block's
+  last row; the per-pair predicate is this reading of it.
 * The softmax scale defaults to ``1/sqrt(D)``. Query head ``h`` reads KV head
   ``h // (Hq/Hkv)``.
 * fp8 caches hold OCP E4M3 "fn" codes (no infinities, S.1111.111 is NaN). The value is
   ``decode(code) * scale``, with one fp32 scale for K and one for V.
-* KV append (the step before attention in chunked prefill, PR #54194 "功能与动机": the
-  new tokens' K/V land in the paged cache): new token ``j`` of sequence ``b`` is written
-  to position ``c + j`` of the sequence, i.e. page ``block_table[b][(c + j) // P]``, slot
+* KV append. The PR #54194 report ("实现拆解" item 4) validates the kernel on a
+  ``k=None`` cache-sourced path, where the new tokens' K/V are read from the paged cache;
+  the pages print no code that writes them there, so the append is a reading: new token
+  ``j`` of sequence ``b`` is written to position ``c + j`` of the sequence, i.e. page ``block_table[b][(c + j) // P]``, slot
   ``(c + j) % P``. A bf16 cache takes the value unchanged. An fp8 cache takes the code
   nearest to ``value / scale`` (the quotient formed in fp32), ties to the even code,
   magnitudes past 448 saturated to 448, NaN to a NaN code. The pages name only the dtype,
@@ -116,13 +124,20 @@ def e4m3fn_encode(x) -> np.ndarray:
 # ---------------------------------------------------------------------------------------
 # The mask.
 # ---------------------------------------------------------------------------------------
+def _chunk_first_key(q, chunk_size: int, chunk_lookback: int):
+    """First key of the chunk ``chunk_lookback`` chunks before query ``q``'s own chunk."""
+    return ((q // chunk_size) - chunk_lookback) * chunk_size
+
+
 def allowed_pair(q: int, k: int, s: int, causal: bool, window_left: int, window_right: int,
-                 ranges: Optional[Iterable], clamp: bool) -> bool:
+                 ranges: Optional[Iterable], clamp: bool, chunk_size: int = 0,
+                 chunk_lookback: int = 0) -> bool:
     """Whether query position ``q`` may attend to key position ``k`` (scalar form).
 
     base: causal ``k <= q`` (else ``k - q < WR`` when ``WR > 0``), and ``q - k < WL``
-    when ``WL > 0``. mm: some valid range contains both q and k (clamped by ``WL`` when
-    ``clamp``). The result is base OR mm.
+    when ``WL > 0`` (with ``chunk_size > 0``: ``k >= ((q // CS) - LB) * CS`` instead). mm:
+    some valid range contains both q and k (clamped by ``WL`` when ``clamp``). The result is
+    base OR mm.
     """
     if k < 0 or k >= s or q < 0 or q >= s:
         return False
@@ -130,7 +145,10 @@ def allowed_pair(q: int, k: int, s: int, causal: bool, window_left: int, window_
         right_ok = k <= q
     else:
         right_ok = window_right <= 0 or (k - q) < window_right
-    left_ok = window_left <= 0 or (q - k) < window_left
+    if chunk_size > 0:
+        left_ok = k >= _chunk_first_key(q, chunk_size, chunk_lookback)
+    else:
+        left_ok = window_left <= 0 or (q - k) < window_left
     if right_ok and left_ok:
         return True
     if ranges is None:
@@ -148,7 +166,8 @@ def allowed_pair(q: int, k: int, s: int, causal: bool, window_left: int, window_
 
 
 def allowed_mask(q_pos: np.ndarray, s: int, causal: bool, window_left: int, window_right: int,
-                 ranges: Optional[np.ndarray], clamp: bool) -> np.ndarray:
+                 ranges: Optional[np.ndarray], clamp: bool, chunk_size: int = 0,
+                 chunk_lookback: int = 0) -> np.ndarray:
     """Dense ``[len(q_pos), s]`` boolean mask, the same predicate as :func:`allowed_pair`."""
     qq = np.asarray(q_pos, dtype=np.int64)[:, None]
     kk = np.arange(s, dtype=np.int64)[None, :]
@@ -158,7 +177,9 @@ def allowed_mask(q_pos: np.ndarray, s: int, causal: bool, window_left: int, wind
         right_ok = (kk - qq) < window_right
     else:
         right_ok = np.ones((1, s), dtype=bool)
-    if window_left > 0:
+    if chunk_size > 0:
+        left_ok = kk >= _chunk_first_key(qq, chunk_size, chunk_lookback)
+    elif window_left > 0:
         left_ok = (qq - kk) < window_left
     else:
         left_ok = np.ones((1, s), dtype=bool)
@@ -213,6 +234,12 @@ def _seq_ranges(inp: dict, b: int) -> Optional[np.ndarray]:
     return None if mm is None else mm[b]
 
 
+def _chunk(inp: dict) -> dict:
+    """The chunked-local parameters of a batch (absent: off)."""
+    return {"chunk_size": int(inp.get("chunk_size", 0) or 0),
+            "chunk_lookback": int(inp.get("chunk_lookback", 0) or 0)}
+
+
 def _scale(inp: dict) -> float:
     sm = inp["sm_scale"]
     return sm if sm > 0 else 1.0 / math.sqrt(inp["head_dim"])
@@ -241,7 +268,7 @@ def attention_rows(inp: dict, b: int, tokens: np.ndarray, dtype=np.float32,
     K, V = kv if kv is not None else (gather_kv(inp, b, "k", dtype), gather_kv(inp, b, "v", dtype))
     tokens = np.asarray(tokens, dtype=np.int64)
     mask = allowed_mask(c + tokens, s, inp["causal"], inp["window_left"], inp["window_right"],
-                        _seq_ranges(inp, b), inp["clamp_mm"])
+                        _seq_ranges(inp, b), inp["clamp_mm"], **_chunk(inp))
     Q = inp["q"][int(cu[b]) + tokens].astype(dtype)  # [t, Hq, D]
     scale = dtype(_scale(inp))
     out = np.empty((len(tokens), Hq, D), dtype=dtype)
@@ -318,7 +345,8 @@ def tile_bounds(inp: dict, tq: int, tn: int) -> np.ndarray:
         for t in range(-(-n // tq)):
             toks = np.arange(t * tq, min(n, (t + 1) * tq))
             mask = allowed_mask(c + toks, s, inp["causal"], inp["window_left"],
-                                inp["window_right"], _seq_ranges(inp, b), inp["clamp_mm"])
+                                inp["window_right"], _seq_ranges(inp, b), inp["clamp_mm"],
+                                **_chunk(inp))
             live = np.nonzero(mask.any(axis=0))[0]
             out.append((live.min() // tn, live.max() // tn + 1))
     return np.asarray(out, dtype=np.int32).reshape(-1, 2)
@@ -335,5 +363,5 @@ def live_pairs(inp: dict, row_chunk: int = 2048) -> int:
             toks = np.arange(j0, min(n, j0 + row_chunk))
             total += int(allowed_mask(c + toks, c + n, inp["causal"], inp["window_left"],
                                       inp["window_right"], _seq_ranges(inp, b),
-                                      inp["clamp_mm"]).sum())
+                                      inp["clamp_mm"], **_chunk(inp)).sum())
     return total

@@ -64,6 +64,8 @@ class PrefillCase:
     cu_query_lens: torch.Tensor
     context_lens: torch.Tensor
     mm_ranges: Optional[torch.Tensor]
+    chunk_size: int = 0      # > 0: chunked-local attention (base left edge at a chunk start)
+    chunk_lookback: int = 0  # chunks before the query's own chunk that stay visible
 
     @property
     def num_seqs(self) -> int:
@@ -132,6 +134,8 @@ class PrefillCase:
             "window_right": self.window_right,
             "clamp_mm": self.clamp_mm,
             "sm_scale": self.sm_scale,
+            "chunk_size": self.chunk_size,
+            "chunk_lookback": self.chunk_lookback,
             "kv_dtype": self.kv_dtype,
             "k_scale": self.k_scale,
             "v_scale": self.v_scale,
@@ -176,6 +180,8 @@ def build_case(
     spare_frac: float = 0.10,
     poison: bool = True,
     value_rng_seed: Optional[int] = None,
+    chunk_size: int = 0,
+    chunk_lookback: int = 0,
 ) -> PrefillCase:
     """Build one case. Lengths are per sequence; ``mm_ranges`` is ``[B, R, 2]`` or None."""
     ctx = np.asarray(context_lens, dtype=np.int64)
@@ -272,6 +278,8 @@ def build_case(
         cu_query_lens=torch.from_numpy(cu.astype(np.int32)),
         context_lens=torch.from_numpy(ctx.astype(np.int32)),
         mm_ranges=mm,
+        chunk_size=int(chunk_size),
+        chunk_lookback=int(chunk_lookback),
     )
 
 

@@ -466,3 +466,60 @@ def test_append_fp8_stores_the_encoded_quotient():
         codes = ref.e4m3fn_encode(x / np.float32(inp["k_scale"]))
         assert np.array_equal(K[c:], ref.e4m3fn_table()[codes.astype(np.int64)] * inp["k_scale"])
         assert np.array_equal(K[:c], ref.gather_kv(inp, b, "k", np.float64)[:c])
+
+
+# ---------------------------------------------------------------------------------------
+# chunked-local attention (base left edge at the start of the chunk LB chunks back)
+# ---------------------------------------------------------------------------------------
+def test_chunked_mask_vectorised_equals_pairwise_and_rows_stay_intervals():
+    rng = np.random.default_rng(50)
+    for _ in range(200):
+        s, c, causal, wl_, wr, ranges, clamp = _random_geometry(rng)
+        cs, lb = int(rng.choice([1, 3, 8, 16, 64])), int(rng.integers(0, 3))
+        qpos = np.arange(c, s)
+        dense = ref.allowed_mask(qpos, s, causal, wl_, wr, ranges, clamp, cs, lb)
+        brute = np.array([[ref.allowed_pair(int(q), k, s, causal, wl_, wr, ranges, clamp, cs, lb)
+                           for k in range(s)] for q in qpos], dtype=bool).reshape(len(qpos), s)
+        assert (dense == brute).all()
+        for i, q in enumerate(qpos):
+            live = np.nonzero(dense[i])[0]
+            assert dense[i, q] and live.max() - live.min() + 1 == live.size
+
+
+def test_chunked_mask_textbook_cases():
+    s = 50
+    q = np.arange(s)
+    causal = np.tril(np.ones((s, s), bool))
+    # chunk 16, lookback 0: block-diagonal causal (each query sees its own chunk's prefix)
+    m = ref.allowed_mask(q, s, True, 0, 0, None, False, 16, 0)
+    blocks = (q[:, None] // 16) == (q[None, :] // 16)
+    assert (m == (causal & blocks)).all()
+    # lookback 1: position 37 sees keys 16 .. 37
+    m1 = ref.allowed_mask(np.array([37]), s, True, 0, 0, None, False, 16, 1)
+    assert np.nonzero(m1[0])[0].tolist() == list(range(16, 38))
+    # a chunk at least as long as the sequence leaves the causal mask
+    assert (ref.allowed_mask(q, s, True, 0, 0, None, False, 64, 0) == causal).all()
+    # chunk 1: only the diagonal; the window_left is not part of the base mask then
+    assert (ref.allowed_mask(q, s, True, 9, 0, None, False, 1, 0) == np.eye(s, dtype=bool)).all()
+    # a clamped MM range re-enables keys before the chunk start (32), down to the window edge
+    # (40 - 12 + 1 = 29, so the range start 30 binds) and up to the range end
+    mm = ref.allowed_mask(np.array([40]), s, True, 12, 0, np.array([[30, 45]]), True, 16, 0)
+    assert np.nonzero(mm[0])[0].tolist() == list(range(30, 46))
+    # with a narrower window the clamped range starts inside the chunk: the chunk edge binds
+    mm6 = ref.allowed_mask(np.array([40]), s, True, 6, 0, np.array([[30, 45]]), True, 16, 0)
+    assert np.nonzero(mm6[0])[0].tolist() == list(range(32, 46))
+
+
+def test_chunk_of_one_returns_each_querys_own_value_row():
+    """With chunk size 1 and no lookback each causal query sees only itself: the output is
+    its own V row, for every head of the group."""
+    case = wl.build_case("t", [5, 0], [9, 12], 4, 2, 16, 8, causal=True, seed=51,
+                         chunk_size=1, chunk_lookback=0)
+    inp = _inp(case)
+    out = ref.attention(inp, np.float64)
+    cu = inp["cu_query_lens"]
+    for b, c in enumerate([5, 0]):
+        V = ref.gather_kv(inp, b, "v", np.float64)
+        for j in range(int(cu[b + 1] - cu[b])):
+            for h in range(4):
+                assert np.allclose(out[int(cu[b]) + j, h], V[c + j, h // 2], rtol=0, atol=1e-12)
