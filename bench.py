@@ -1,7 +1,7 @@
 """Benchmark: chunked-prefill attention over a paged KV cache on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached] [--no-cpu-baseline]
+                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached|chunked] [--no-cpu-baseline]
                     [--sweep windows]
 
 A step is one pass of the whole hot path over one batch: for every shape of the workload,
@@ -62,6 +62,9 @@ def make_workload(name: str, seed: int):
         return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
                 "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
                 [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
+    if name == "chunked":
+        return ("chunked-local attention: 4 seqs x 32768 new tokens, 32 q / 8 kv heads, D 128, "
+                "page 544, causal, chunk 8192, lookback 0", [wl.chunked_local(seed=seed)])
     if name == "mixed_cached":
         return ("mixed serving, new tokens appended to the paged cache then attended from it "
                 "(ppa_append_kv + cache-sourced attention): 32 seqs, ctx U[4096,32768], "
@@ -308,7 +311,8 @@ def oracle_sample(cases, budget_s: float, rng_seed: int = 0):
             dt = time.perf_counter() - t0
             pairs = int(ref.allowed_mask(c + toks, c + n, case.causal, case.window_left,
                                          case.window_right, None if inp["mm_ranges"] is None
-                                         else inp["mm_ranges"][b], case.clamp_mm).sum())
+                                         else inp["mm_ranges"][b], case.clamp_mm,
+                                         case.chunk_size, case.chunk_lookback).sum())
             flops += 4.0 * case.head_dim * case.num_q_heads * pairs
             secs += dt
             tokens += len(toks)

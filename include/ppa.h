@@ -98,6 +98,13 @@ typedef struct {
   int kv_dtype;          /* PPA_KV_BF16 or PPA_KV_FP8_E4M3 */
   unsigned flags;        /* PPA_FLAG_* */
   float sm_scale;        /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+  int chunk_size;        /* > 0: chunked-local attention, 0: off. The base mask's left edge is
+                          * k >= ((q / chunk_size) - chunk_lookback) * chunk_size instead of the
+                          * left window (window_left then only clamps multimodal ranges); the
+                          * CHUNK_LOOKBACK branch of compute_tile_loop_bounds, "[Kernel][Gemma4]
+                          * Prune Triton sliding-window tiles for multimodal prefixes",
+                          * 关键源码片段, read per pair */
+  int chunk_lookback;    /* >= 0: earlier chunks that stay visible (with chunk_size > 0) */
 } ppa_dims;
 
 /* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list; with

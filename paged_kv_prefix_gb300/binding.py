@@ -46,6 +46,8 @@ class PpaDims(ctypes.Structure):
         ("kv_dtype", ctypes.c_int),
         ("flags", ctypes.c_uint),
         ("sm_scale", ctypes.c_float),
+        ("chunk_size", ctypes.c_int),
+        ("chunk_lookback", ctypes.c_int),
     ]
 
 
@@ -273,7 +275,8 @@ def dims_for(case, flags_extra: int = 0) -> PpaDims:
         max_mm_ranges=case.max_mm_ranges, window_left=case.window_left,
         window_right=case.window_right,
         kv_dtype=PPA_KV_FP8_E4M3 if case.kv_dtype == "fp8_e4m3" else PPA_KV_BF16,
-        flags=flags | flags_extra, sm_scale=case.sm_scale)
+        flags=flags | flags_extra, sm_scale=case.sm_scale,
+        chunk_size=getattr(case, "chunk_size", 0), chunk_lookback=getattr(case, "chunk_lookback", 0))
 
 
 class DeviceCase:

@@ -34,6 +34,7 @@ ppa_status check_dims(const ppa_dims* d) {
   if (d->num_q_heads % d->num_kv_heads != 0) return PPA_ERR_INVALID;
   if (d->page_size < 1 || d->num_pages < 1 || d->max_pages_per_seq < 1) return PPA_ERR_INVALID;
   if (d->max_mm_ranges < 0) return PPA_ERR_INVALID;
+  if (d->chunk_size < 0 || (d->chunk_size > 0 && d->chunk_lookback < 0)) return PPA_ERR_INVALID;
   if ((d->flags & ~kKnownFlags) != 0u) return PPA_ERR_INVALID;
   if (!std::isfinite(d->sm_scale)) return PPA_ERR_INVALID;
   if (d->kv_dtype != PPA_KV_BF16 && d->kv_dtype != PPA_KV_FP8_E4M3) return PPA_ERR_INVALID;
@@ -59,6 +60,8 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
   m.clamp_mm = (d->flags & PPA_FLAG_CLAMP_MM) ? 1 : 0;
   m.max_mm_ranges = (mm_ranges != nullptr) ? d->max_mm_ranges : 0;
   m.mm_ranges = (d->max_mm_ranges > 0) ? mm_ranges : nullptr;
+  m.chunk_size = d->chunk_size > 0 ? d->chunk_size : 0;
+  m.chunk_lookback = d->chunk_size > 0 ? d->chunk_lookback : 0;
   return m;
 }
 

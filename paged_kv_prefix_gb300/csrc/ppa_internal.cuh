@@ -19,7 +19,17 @@ struct MaskParams {
   int clamp_mm;
   int max_mm_ranges;
   const int32_t* mm_ranges;  // [B][R][2] or nullptr
+  int chunk_size;            // > 0: chunked-local base left edge (instead of window_left)
+  int chunk_lookback;
 };
+
+// Lowest key of the base mask for query position q: the start of the chunk chunk_lookback
+// chunks before q's own (chunked-local attention), else the left window's edge, else 0. The
+// result is non-decreasing in q, so over a run of rows the first row's value bounds them all.
+__device__ __forceinline__ int base_first_key(int q, const MaskParams& mp) {
+  if (mp.chunk_size > 0) return (q / mp.chunk_size - mp.chunk_lookback) * mp.chunk_size;
+  return mp.window_left > 0 ? q - mp.window_left + 1 : 0;
+}
 
 // Workspace header; followed by per-sequence arrays, the unit table and the work list.
 struct WsHeader {
@@ -51,7 +61,7 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
 __device__ __forceinline__ void row_interval(int q, int s, const MaskParams& mp,
                                              const int32_t* ranges /* this sequence, [R][2] */,
                                              int& kmin, int& kmax) {
-  int lo = mp.window_left > 0 ? q - mp.window_left + 1 : 0;
+  int lo = base_first_key(q, mp);
   int hi;
   if (mp.causal) {
     hi = q;
@@ -85,7 +95,7 @@ __device__ __forceinline__ void row_interval(int q, int s, const MaskParams& mp,
 // which is not a bound for the earlier rows of the block).
 __device__ __forceinline__ void tile_interval(int q_lo, int q_hi, int s, const MaskParams& mp,
                                               const int32_t* ranges, int& klo, int& khi) {
-  int lo = mp.window_left > 0 ? q_lo - mp.window_left + 1 : 0;
+  int lo = base_first_key(q_lo, mp);
   int hi;
   if (mp.causal) {
     hi = q_hi;

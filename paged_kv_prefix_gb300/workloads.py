@@ -331,6 +331,16 @@ def swa_causal(seed: int = 0, scale: float = 1.0, seq_len: int = 32768, window: 
                       window_left=window, seed=seed, **kw)
 
 
+def chunked_local(seed: int = 0, scale: float = 1.0, num_seqs: int = 4, seq_len: int = 32768,
+                  chunk: int = 8192, lookback: int = 0, **kw) -> PrefillCase:
+    """Chunked-local prefill: 4 x 32768 new tokens, 32 q / 8 kv heads, D 128, page 544,
+    causal, chunks of 8192 keys (each query sees its own chunk's prefix)."""
+    n = _scaled(seq_len, scale)
+    c = max(1, _scaled(chunk, scale))
+    return build_case(f"chunked{c}_lb{lookback}", [0] * num_seqs, [n] * num_seqs, 32, 8, 128,
+                      544, causal=True, chunk_size=c, chunk_lookback=lookback, seed=seed, **kw)
+
+
 def mm_ranges_for(seq_len: int, num_ranges: int, width: int, rng: np.random.Generator) -> np.ndarray:
     """Non-overlapping ranges [a, a + width - 1] at seeded random starts."""
     free = seq_len - num_ranges * width

@@ -125,6 +125,30 @@ def test_fp8_kv_scales_of_2_8_and_above(head_dim, fp8_path):
     assert_close(got / big, want / big, case.name)
 
 
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("chunk,lookback", [(16, 0), (100, 1), (300, 2)])
+def test_chunked_local_parity(head_dim, causal, chunk, lookback):
+    """Chunked-local attention: the base left edge at a chunk start; key tiles before it are
+    skipped (a chunk boundary inside a query tile keeps the earlier chunk's keys live)."""
+    rng = np.random.default_rng(head_dim + chunk)
+    ctx = [0, int(rng.integers(100, 500)), 37, 300]
+    qlen = [int(rng.integers(200, 420)), int(rng.integers(60, 200)), 1, 129]
+    parity(wl.build_case("chunked", ctx, qlen, 8, 2, head_dim, 37, causal=causal,
+                         window_right=0 if causal else 70, chunk_size=chunk,
+                         chunk_lookback=lookback, seed=chunk))
+
+
+@pytest.mark.parametrize("head_dim", [128, 256])
+def test_chunked_local_with_clamped_mm_ranges(head_dim):
+    """The review case on the multimodal-pruning page: clamped ranges, OR-ed on with the left
+    window as their clamp, re-enable keys before the chunk start."""
+    mm = np.array([[[120, 380], [500, 520]], [[0, 0], [40, 90]]])
+    parity(wl.build_case("chunked_mm", [0, 200], [600, 300], 8, 4, head_dim, 16, causal=True,
+                         window_left=150, mm_ranges=mm, clamp_mm=True, chunk_size=128,
+                         chunk_lookback=0, seed=head_dim))
+
+
 def test_page_permutation_is_bitwise_invariant():
     a = wl.build_case("perm", [300, 1000], [200, 333], 8, 2, 128, 544, causal=True, seed=10,
                       value_rng_seed=77)

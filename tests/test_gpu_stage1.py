@@ -35,9 +35,11 @@ def _geometry_cases():
                 for r in range(R):
                     a = int(rng.integers(-3, s + 5))
                     mm[b, r] = (a, a + int(rng.integers(-2, 90)))
+        chunk = int(rng.choice([0, 0, 1, 16, 100])) if i >= 12 else 0  # chunked-local rows
         cases.append(wl.build_case(f"geo{i}", ctx, qlen, 2, 1, 64, int(rng.choice([5, 16, 37])),
                                    causal=causal, window_left=wl_, window_right=wr,
-                                   mm_ranges=mm, clamp_mm=bool(rng.integers(0, 2)), seed=i))
+                                   mm_ranges=mm, clamp_mm=bool(rng.integers(0, 2)), seed=i,
+                                   chunk_size=chunk, chunk_lookback=int(rng.integers(0, 3))))
     cases.append(wl.build_case("page_fixture", [0], [4096], 2, 1, 64, 16, causal=True,
                                window_left=1024, mm_ranges=np.array([[[1024, 2303], [0, 0]]]),
                                clamp_mm=True))
@@ -71,7 +73,7 @@ def test_tile_bounds_page_worked_example():
     assert out[140].tolist() == [3, 72]
 
 
-@pytest.mark.parametrize("case", _geometry_cases()[:12], ids=lambda c: c.name)
+@pytest.mark.parametrize("case", _geometry_cases()[:12] + _geometry_cases()[12:24:2], ids=lambda c: c.name)
 def test_debug_mask_bit_exact(case):
     inp = case.numpy_inputs()
     dims = binding.dims_for(case)
@@ -90,12 +92,13 @@ def test_debug_mask_bit_exact(case):
         got = ((bits[:, :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(n, words * 32)
         want = ref.allowed_mask(c + np.arange(n), s, case.causal, case.window_left,
                                 case.window_right, None if inp["mm_ranges"] is None
-                                else inp["mm_ranges"][b], case.clamp_mm)
+                                else inp["mm_ranges"][b], case.clamp_mm, case.chunk_size,
+                                case.chunk_lookback)
         assert np.array_equal(got[:, :s].astype(bool), want)
         assert not got[:, s:].any()
 
 
-@pytest.mark.parametrize("case", _geometry_cases()[:12], ids=lambda c: c.name)
+@pytest.mark.parametrize("case", _geometry_cases()[:12] + _geometry_cases()[12:24:2], ids=lambda c: c.name)
 def test_live_pairs_bit_exact(case):
     dims = binding.dims_for(case)
     out = torch.zeros(1, dtype=torch.int64, device="cuda")
@@ -119,7 +122,7 @@ def test_e4m3_decode_bit_exact():
     assert np.array_equal(out2.view(torch.bfloat16).float().cpu().numpy(), table[100:107])
 
 
-@pytest.mark.parametrize("case", _geometry_cases()[:12], ids=lambda c: c.name)
+@pytest.mark.parametrize("case", _geometry_cases()[:12] + _geometry_cases()[12:24:2], ids=lambda c: c.name)
 def test_live_kv_tokens_bit_exact(case):
     """Cached context keys that some query of the sequence may attend to, from the dense mask."""
     inp = case.numpy_inputs()
@@ -131,7 +134,8 @@ def test_live_kv_tokens_bit_exact(case):
             continue
         m = ref.allowed_mask(c + np.arange(n), c + n, case.causal, case.window_left,
                              case.window_right, None if inp["mm_ranges"] is None
-                             else inp["mm_ranges"][b], case.clamp_mm)
+                             else inp["mm_ranges"][b], case.clamp_mm, case.chunk_size,
+                             case.chunk_lookback)
         want += int(m[:, :c].any(axis=0).sum())
     out = torch.zeros(1, dtype=torch.int64, device="cuda")
     binding.ppa_live_kv_tokens(binding.dims_for(case), case.cu_query_lens.cuda(),
