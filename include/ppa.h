@@ -105,6 +105,11 @@ typedef struct {
                           * Prune Triton sliding-window tiles for multimodal prefixes",
                           * 关键源码片段, read per pair */
   int chunk_lookback;    /* >= 0: earlier chunks that stay visible (with chunk_size > 0) */
+  const int32_t* seq_causal; /* NULL, or a device array of num_seqs int32: sequence b's base
+                              * mask is causal iff seq_causal[b] != 0, overriding
+                              * PPA_FLAG_CAUSAL (per-sequence causality, USE_PER_SEQ_CAUSAL on
+                              * the multimodal-pruning page). Read on the device by ppa_plan,
+                              * ppa_attend and the mask/count entry points. */
 } ppa_dims;
 
 /* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list; with

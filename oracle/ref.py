@@ -40,6 +40,10 @@ Readings where the pages are silent or disagree:
   "评论区精华": the MM mask is OR-ed on and clamped by the sliding window, so it can re-enable
   keys before the chunk boundary). The page prints only the tile bound, taken at the block's
   last row; the per-pair predicate is this reading of it.
+* Per-sequence causality (``USE_PER_SEQ_CAUSAL`` on the PR #53147 page, where the tile
+  bound takes the non-causal right edge because causality is decided per sequence inside
+  the mask): ``inp["seq_causal"][b]``, when given, replaces the batch's causal flag for
+  sequence ``b``.
 * The softmax scale defaults to ``1/sqrt(D)``. Query head ``h`` reads KV head
   ``h // (Hq/Hkv)``.
 * fp8 caches hold OCP E4M3 "fn" codes (no infinities, S.1111.111 is NaN). The value is
@@ -234,6 +238,12 @@ def _seq_ranges(inp: dict, b: int) -> Optional[np.ndarray]:
     return None if mm is None else mm[b]
 
 
+def _causal(inp: dict, b: int) -> bool:
+    """Whether sequence ``b``'s base mask is causal."""
+    sc = inp.get("seq_causal")
+    return bool(inp["causal"]) if sc is None else bool(sc[b])
+
+
 def _chunk(inp: dict) -> dict:
     """The chunked-local parameters of a batch (absent: off)."""
     return {"chunk_size": int(inp.get("chunk_size", 0) or 0),
@@ -267,7 +277,7 @@ def attention_rows(inp: dict, b: int, tokens: np.ndarray, dtype=np.float32,
     s = c + n
     K, V = kv if kv is not None else (gather_kv(inp, b, "k", dtype), gather_kv(inp, b, "v", dtype))
     tokens = np.asarray(tokens, dtype=np.int64)
-    mask = allowed_mask(c + tokens, s, inp["causal"], inp["window_left"], inp["window_right"],
+    mask = allowed_mask(c + tokens, s, _causal(inp, b), inp["window_left"], inp["window_right"],
                         _seq_ranges(inp, b), inp["clamp_mm"], **_chunk(inp))
     Q = inp["q"][int(cu[b]) + tokens].astype(dtype)  # [t, Hq, D]
     scale = dtype(_scale(inp))
@@ -344,7 +354,7 @@ def tile_bounds(inp: dict, tq: int, tn: int) -> np.ndarray:
         s = c + n
         for t in range(-(-n // tq)):
             toks = np.arange(t * tq, min(n, (t + 1) * tq))
-            mask = allowed_mask(c + toks, s, inp["causal"], inp["window_left"],
+            mask = allowed_mask(c + toks, s, _causal(inp, b), inp["window_left"],
                                 inp["window_right"], _seq_ranges(inp, b), inp["clamp_mm"],
                                 **_chunk(inp))
             live = np.nonzero(mask.any(axis=0))[0]
@@ -361,7 +371,7 @@ def live_pairs(inp: dict, row_chunk: int = 2048) -> int:
         n = int(cu[b + 1] - cu[b])
         for j0 in range(0, n, row_chunk):
             toks = np.arange(j0, min(n, j0 + row_chunk))
-            total += int(allowed_mask(c + toks, c + n, inp["causal"], inp["window_left"],
+            total += int(allowed_mask(c + toks, c + n, _causal(inp, b), inp["window_left"],
                                       inp["window_right"], _seq_ranges(inp, b),
                                       inp["clamp_mm"], **_chunk(inp)).sum())
     return total

@@ -48,6 +48,7 @@ class PpaDims(ctypes.Structure):
         ("sm_scale", ctypes.c_float),
         ("chunk_size", ctypes.c_int),
         ("chunk_lookback", ctypes.c_int),
+        ("seq_causal", ctypes.c_void_p),  # device int32[num_seqs] or None
     ]
 
 
@@ -296,6 +297,10 @@ class DeviceCase:
         self.cu_query_lens = case.cu_query_lens.to(dev)
         self.context_lens = case.context_lens.to(dev)
         self.mm_ranges = None if case.mm_ranges is None else case.mm_ranges.to(dev)
+        seq_causal = getattr(case, "seq_causal", None)
+        self.seq_causal = None if seq_causal is None else seq_causal.to(dev)
+        if self.seq_causal is not None:
+            self.dims.seq_causal = self.seq_causal.data_ptr()
         self.k_scale = torch.tensor([case.k_scale], dtype=torch.float32, device=dev)
         self.v_scale = torch.tensor([case.v_scale], dtype=torch.float32, device=dev)
         self.out = torch.zeros_like(self.q)

@@ -62,6 +62,7 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
   m.mm_ranges = (d->max_mm_ranges > 0) ? mm_ranges : nullptr;
   m.chunk_size = d->chunk_size > 0 ? d->chunk_size : 0;
   m.chunk_lookback = d->chunk_size > 0 ? d->chunk_lookback : 0;
+  m.seq_causal = d->seq_causal;
   return m;
 }
 

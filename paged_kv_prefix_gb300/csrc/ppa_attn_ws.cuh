@@ -190,7 +190,7 @@ __device__ __forceinline__ void row_bounds_of(const AttnParams& p, const UnitInf
     kmin = kb.x;
     kmax = kb.y;
   } else {
-    row_interval(u.c + j, u.s, p.mask, nullptr, kmin, kmax);
+    row_interval(u.c + j, u.s, seq_mask(p.mask, u.b), nullptr, kmin, kmax);
   }
 }
 

@@ -21,7 +21,15 @@ struct MaskParams {
   const int32_t* mm_ranges;  // [B][R][2] or nullptr
   int chunk_size;            // > 0: chunked-local base left edge (instead of window_left)
   int chunk_lookback;
+  const int32_t* seq_causal;  // [B] per-sequence causal flags, or nullptr (use `causal`)
 };
+
+// The mask of sequence b: `causal` taken from the per-sequence flags when given.
+__device__ __forceinline__ MaskParams seq_mask(const MaskParams& mp, int b) {
+  MaskParams m = mp;
+  if (mp.seq_causal != nullptr) m.causal = mp.seq_causal[b] != 0 ? 1 : 0;
+  return m;
+}
 
 // Lowest key of the base mask for query position q: the start of the chunk chunk_lookback
 // chunks before q's own (chunked-local attention), else the left window's edge, else 0. The

@@ -82,7 +82,7 @@ __device__ __forceinline__ void qtile_bounds(const Stage1Params& p, int seq, int
   const int32_t* ranges =
       p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)seq * p.mask.max_mm_ranges * 2 : nullptr;
   int klo, khi;
-  tile_interval(q_lo, q_hi, s, p.mask, ranges, klo, khi);
+  tile_interval(q_lo, q_hi, s, seq_mask(p.mask, seq), ranges, klo, khi);
   *lo = klo / p.tn;
   *hi = khi / p.tn + 1;
 }
@@ -278,7 +278,7 @@ __global__ void debug_mask_kernel(const MaskParams mp, int seq, const int32_t* c
   const int32_t* ranges = mp.mm_ranges ? mp.mm_ranges + (size_t)seq * mp.max_mm_ranges * 2 : nullptr;
   for (int j = blockIdx.x; j < rows; j += gridDim.x) {
     int kmin, kmax;
-    row_interval(c + j, s, mp, ranges, kmin, kmax);
+    row_interval(c + j, s, seq_mask(mp, seq), ranges, kmin, kmax);
     for (int w = threadIdx.x; w < words_per_row; w += blockDim.x) {
       const int k0 = w * 32;
       uint32_t bits = 0;
@@ -309,7 +309,7 @@ __global__ void live_pairs_kernel(const MaskParams mp, int num_seqs, int total_q
     if (j < 0 || j >= n) continue;
     const int32_t* ranges = mp.mm_ranges ? mp.mm_ranges + (size_t)b * mp.max_mm_ranges * 2 : nullptr;
     int kmin, kmax;
-    row_interval(c + j, c + n, mp, ranges, kmin, kmax);
+    row_interval(c + j, c + n, seq_mask(mp, b), ranges, kmin, kmax);
     acc += (unsigned long long)(kmax - kmin + 1);
   }
 #pragma unroll
@@ -336,7 +336,7 @@ __global__ void row_bounds_kernel(const MaskParams mp, int num_seqs, int total_q
     const int j = tok - cu[b];
     const int32_t* ranges = mp.mm_ranges ? mp.mm_ranges + (size_t)b * mp.max_mm_ranges * 2 : nullptr;
     int kmin = 0, kmax = 0;
-    if (j >= 0 && j < n) row_interval(c + j, c + n, mp, ranges, kmin, kmax);
+    if (j >= 0 && j < n) row_interval(c + j, c + n, seq_mask(mp, b), ranges, kmin, kmax);
     out[2 * (size_t)tok] = kmin;
     out[2 * (size_t)tok + 1] = kmax;
   }
@@ -355,7 +355,7 @@ __global__ void live_kv_tokens_kernel(const MaskParams mp, const int32_t* cu, co
   int lo = INT_MAX, hi = INT_MIN;
   for (int j = threadIdx.x; j < n; j += blockDim.x) {
     int kmin, kmax;
-    row_interval(c + j, c + n, mp, ranges, kmin, kmax);
+    row_interval(c + j, c + n, seq_mask(mp, b), ranges, kmin, kmax);
     lo = min(lo, kmin);
     hi = max(hi, kmax);
   }

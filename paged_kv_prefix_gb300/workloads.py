@@ -66,6 +66,7 @@ class PrefillCase:
     mm_ranges: Optional[torch.Tensor]
     chunk_size: int = 0      # > 0: chunked-local attention (base left edge at a chunk start)
     chunk_lookback: int = 0  # chunks before the query's own chunk that stay visible
+    seq_causal: Optional[torch.Tensor] = None  # int32 [B]: per-sequence causal flags
 
     @property
     def num_seqs(self) -> int:
@@ -136,6 +137,7 @@ class PrefillCase:
             "sm_scale": self.sm_scale,
             "chunk_size": self.chunk_size,
             "chunk_lookback": self.chunk_lookback,
+            "seq_causal": None if self.seq_causal is None else self.seq_causal.numpy().astype(bool),
             "kv_dtype": self.kv_dtype,
             "k_scale": self.k_scale,
             "v_scale": self.v_scale,
@@ -182,6 +184,7 @@ def build_case(
     value_rng_seed: Optional[int] = None,
     chunk_size: int = 0,
     chunk_lookback: int = 0,
+    seq_causal: Optional[Sequence[bool]] = None,
 ) -> PrefillCase:
     """Build one case. Lengths are per sequence; ``mm_ranges`` is ``[B, R, 2]`` or None."""
     ctx = np.asarray(context_lens, dtype=np.int64)
@@ -280,6 +283,8 @@ def build_case(
         mm_ranges=mm,
         chunk_size=int(chunk_size),
         chunk_lookback=int(chunk_lookback),
+        seq_causal=None if seq_causal is None
+        else torch.tensor([1 if x else 0 for x in seq_causal], dtype=torch.int32),
     )
 
 

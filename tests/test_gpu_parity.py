@@ -206,3 +206,35 @@ def test_status_reports_bad_lengths():
     dc.run()
     torch.cuda.synchronize()
     assert dc.read_status() == binding.PPA_ERR_INVALID
+
+
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("windowed", [False, True])
+def test_per_sequence_causal_parity(head_dim, windowed):
+    """Per-sequence causal flags: each sequence's key tiles and mask follow its own flag."""
+    rng = np.random.default_rng(head_dim + windowed)
+    ctx = [0, int(rng.integers(50, 300)), 130, 0]
+    qlen = [int(rng.integers(150, 300)), int(rng.integers(40, 150)), 77, 129]
+    parity(wl.build_case("seq_causal", ctx, qlen, 8, 4, head_dim, 16, causal=True,
+                         window_left=120 if windowed else 0, window_right=60 if windowed else 0,
+                         seq_causal=[True, False, False, True], seed=head_dim))
+
+
+def test_per_sequence_causal_with_ranges_and_tile_bounds():
+    mm = np.array([[[30, 90]], [[10, 200]], [[0, 0]]])
+    case = wl.build_case("seq_causal_mm", [0, 40, 10], [300, 250, 90], 8, 2, 128, 37, causal=False,
+                         window_left=64, window_right=32, mm_ranges=mm, clamp_mm=True,
+                         seq_causal=[False, True, True], seed=7)
+    parity(case)
+    # the plan's per-tile bounds follow each sequence's flag, bit-exact
+    dims = binding.dims_for(case)
+    sc = case.seq_causal.cuda()
+    dims.seq_causal = sc.data_ptr()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cap = -(-case.total_q // 16) + case.num_seqs
+    out = torch.full((cap, 2), -7, dtype=torch.int32, device="cuda")
+    binding.ppa_tile_bounds(dims, 16, 128, case.cu_query_lens.cuda(), case.context_lens.cuda(),
+                            case.mm_ranges.cuda(), out, status)
+    assert binding.ppa_read_status(status) == 0
+    want = ref.tile_bounds(case.numpy_inputs(), 16, 128)
+    assert np.array_equal(out[: len(want)].cpu().numpy(), want)

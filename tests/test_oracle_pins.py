@@ -523,3 +523,19 @@ def test_chunk_of_one_returns_each_querys_own_value_row():
         for j in range(int(cu[b + 1] - cu[b])):
             for h in range(4):
                 assert np.allclose(out[int(cu[b]) + j, h], V[c + j, h // 2], rtol=0, atol=1e-12)
+
+
+def test_per_sequence_causal_flags_select_each_sequences_mask():
+    """A batch with per-sequence flags [causal, non-causal, causal] gives, row for row, the
+    output of the same batch run all-causal for sequences 0 and 2 and all-non-causal for 1."""
+    import dataclasses
+    base = wl.build_case("t", [7, 20, 0], [15, 9, 11], 4, 2, 16, 8, causal=True,
+                         window_right=5, seed=52)
+    mixed = dataclasses.replace(base, seq_causal=torch.tensor([1, 0, 1], dtype=torch.int32))
+    out = ref.attention(_inp(mixed), np.float64)
+    all_c = ref.attention(_inp(base), np.float64)
+    all_n = ref.attention(_inp(dataclasses.replace(base, causal=False)), np.float64)
+    assert not np.allclose(all_c, all_n)
+    rows = [(0, 15, all_c), (15, 24, all_n), (24, 35, all_c)]
+    for a, e, want in rows:
+        assert np.array_equal(out[a:e], want[a:e])
