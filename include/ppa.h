@@ -251,7 +251,10 @@ ppa_status ppa_read_status(int32_t* device_status, void* stream);
 /* Static text for a status code. */
 const char* ppa_status_string(ppa_status status);
 
-/* Library version (major * 10000 + minor * 100 + patch). */
+/* Library version (major * 10000 + minor * 100 + patch). 0.2.0 added ppa_append_kv, the
+ * PPA_FLAG_FP8_INKERNEL and PPA_FLAG_KV_IN_CACHE flags, and the ppa_dims fields chunk_size,
+ * chunk_lookback and seq_causal (a layout change: callers built against 0.1 must rebuild). */
+#define PPA_VERSION 200
 int ppa_version(void);
 
 #ifdef __cplusplus

@@ -507,6 +507,6 @@ const char* ppa_status_string(ppa_status status) {
   return "unknown status";
 }
 
-int ppa_version(void) { return 100; }
+int ppa_version(void) { return PPA_VERSION; }
 
 }  // extern "C"
