@@ -1,7 +1,8 @@
 """Benchmark: chunked-prefill attention over a paged KV cache on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached|chunked] [--no-cpu-baseline]
+                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached|chunked|
+                                decode|decode_split] [--no-cpu-baseline]
                     [--sweep windows]
 
 A step is one pass of the whole hot path over one batch: for every shape of the workload,
@@ -62,6 +63,11 @@ def make_workload(name: str, seed: int):
         return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
                 "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
                 [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
+    if name in ("decode", "decode_split"):
+        return (f"decode: 32 seqs, ctx U[8192,32768], 1 new token each, 32 q / 8 kv heads, D 128, "
+                f"page 544, causal"
+                + (", split-KV in segments of 16 key tiles" if name == "decode_split" else ""),
+                [wl.decode(seed=seed)])
     if name == "chunked":
         return ("chunked-local attention: 4 seqs x 32768 new tokens, 32 q / 8 kv heads, D 128, "
                 "page 544, causal, chunk 8192, lookback 0", [wl.chunked_local(seed=seed)])
@@ -95,8 +101,10 @@ def _kv_in_cache(dc) -> bool:
 
 def _launches_per_step(dc) -> int:
     """Kernels of this library per step: the plan and the attention kernel, plus the fp8
-    live-tile marking and dequantisation kernels, plus the KV append."""
-    return 2 + (2 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
+    live-tile marking and dequantisation kernels, plus the KV append, plus the split-KV
+    merge."""
+    return (2 + (2 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
+            + (1 if dc.dims.kv_split_tiles > 0 else 0))
 
 
 def workload_flags(name: str) -> int:
@@ -371,7 +379,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     binding.lib()
     desc, cases = make_workload(args.workload, seed=rank)
-    dcs = [binding.DeviceCase(c, device=dev, flags_extra=workload_flags(args.workload))
+    dcs = [binding.DeviceCase(c, device=dev, flags_extra=workload_flags(args.workload),
+                              kv_split_tiles=16 if args.workload == "decode_split" else 0)
            for c in cases]
     stream = torch.cuda.current_stream(dev)
 
@@ -463,7 +472,8 @@ def run_ours(args):
     roof = roofline(flops[dom], nbytes[dom], dom_avg_s, peaks, peak_src)
     roof["traffic"] = recorded_traffic(args.workload)
     roof["kernel"] = (f"{'fp8 dequant + ' if _prepass(dcs[dom]) else ''}"
-                      f"{'attn_pair_kernel' if cases[dom].head_dim == 256 else 'attn_ws_kernel'} "
+                      f"{'attn_pair_kernel' if cases[dom].head_dim == 256 else 'attn_ws_kernel'}"
+                      f"{' + split merge' if dcs[dom].dims.kv_split_tiles > 0 else ''} "
                       f"({cases[dom].name})")
     shapes = []
     for i, case in enumerate(cases):

@@ -105,6 +105,12 @@ typedef struct {
                           * Prune Triton sliding-window tiles for multimodal prefixes",
                           * 关键源码片段, read per pair */
   int chunk_lookback;    /* >= 0: earlier chunks that stay visible (with chunk_size > 0) */
+  int kv_split_tiles;    /* > 0: split-KV. A sequence whose new tokens fit one query tile
+                          * (decode, speculative verification) and whose live keys span more
+                          * than this many 128-key tiles is cut into segments of this many
+                          * tiles, attended in parallel and merged by their log-sum-exps
+                          * (the segmented mode the PR #53147 page names, tiles_per_segment).
+                          * 0: off. The workspace then holds the partial results. */
   const int32_t* seq_causal; /* NULL, or a device array of num_seqs int32: sequence b's base
                               * mask is causal iff seq_causal[b] != 0, overriding
                               * PPA_FLAG_CAUSAL (per-sequence causality, USE_PER_SEQ_CAUSAL on

@@ -48,6 +48,7 @@ class PpaDims(ctypes.Structure):
         ("sm_scale", ctypes.c_float),
         ("chunk_size", ctypes.c_int),
         ("chunk_lookback", ctypes.c_int),
+        ("kv_split_tiles", ctypes.c_int),
         ("seq_causal", ctypes.c_void_p),  # device int32[num_seqs] or None
     ]
 
@@ -283,10 +284,11 @@ def dims_for(case, flags_extra: int = 0) -> PpaDims:
 class DeviceCase:
     """A case's tensors on the GPU plus the output, workspace and status buffers."""
 
-    def __init__(self, case, device="cuda", flags_extra: int = 0):
+    def __init__(self, case, device="cuda", flags_extra: int = 0, kv_split_tiles: int = 0):
         import torch
         self.case = case
         self.dims = dims_for(case, flags_extra)
+        self.dims.kv_split_tiles = kv_split_tiles  # sizes the workspace below
         dev = torch.device(device)
         self.q = case.q.to(dev)
         self.k_new = case.k_new.to(dev)

@@ -35,6 +35,7 @@ ppa_status check_dims(const ppa_dims* d) {
   if (d->page_size < 1 || d->num_pages < 1 || d->max_pages_per_seq < 1) return PPA_ERR_INVALID;
   if (d->max_mm_ranges < 0) return PPA_ERR_INVALID;
   if (d->chunk_size < 0 || (d->chunk_size > 0 && d->chunk_lookback < 0)) return PPA_ERR_INVALID;
+  if (d->kv_split_tiles < 0) return PPA_ERR_INVALID;
   if ((d->flags & ~kKnownFlags) != 0u) return PPA_ERR_INVALID;
   if (!std::isfinite(d->sm_scale)) return PPA_ERR_INVALID;
   if (d->kv_dtype != PPA_KV_BF16 && d->kv_dtype != PPA_KV_FP8_E4M3) return PPA_ERR_INVALID;
@@ -68,6 +69,10 @@ ppa::MaskParams mask_of(const ppa_dims* d, const int32_t* mm_ranges) {
 
 struct WsLayout {
   size_t header, seq_unit_base, seq_cost, seq_order, seq_item_base, units, items;
+  // split-KV: unit capacity with the segments, per-sequence partial-slot bases, partials
+  long long max_units;
+  bool split;
+  size_t seq_split_base, part_o, part_lse;
   size_t row_bounds;  // [total_q][2] row intervals; only with multimodal ranges
   bool has_row_bounds;
   // fp8 caches dequantised before the attention kernel (see ppa_fp8_dequant.cu)
@@ -86,9 +91,29 @@ WsLayout ws_layout(const ppa_dims* d) {
   w.seq_cost = align_up(w.seq_unit_base + seq_ints * 4, 256);
   w.seq_order = align_up(w.seq_cost + seq_ints * 4, 256);
   w.seq_item_base = align_up(w.seq_order + seq_ints * 4, 256);
+  // split-KV: a split sequence has one query tile (n <= tq) and at most
+  // ceil((max_pages_per_seq * P + tq) / 128) key tiles, so at most nseg_max segments
+  long long nseg_max = 1;
+  w.split = d->kv_split_tiles > 0;
+  if (w.split) {
+    const long long tn = ppa::keys_per_tile(d->head_dim);
+    const long long tq = ppa::tokens_per_qtile(group_of(d));
+    const long long tiles = ((long long)d->max_pages_per_seq * d->page_size + tq + tn - 1) / tn;
+    nseg_max = (tiles + d->kv_split_tiles - 1) / d->kv_split_tiles;
+    if (nseg_max < 1) nseg_max = 1;
+  }
+  w.max_units = mq + (w.split ? (long long)d->num_seqs * (nseg_max - 1) : 0);
   w.units = align_up(w.seq_item_base + seq_ints * 4, 256);
-  w.items = align_up(w.units + (size_t)mq * sizeof(ppa::Unit), 256);
-  w.total = align_up(w.items + (size_t)mq * d->num_kv_heads * 4, 256);
+  w.items = align_up(w.units + (size_t)w.max_units * sizeof(ppa::Unit), 256);
+  w.total = align_up(w.items + (size_t)w.max_units * d->num_kv_heads * 4, 256);
+  w.seq_split_base = w.part_o = w.part_lse = w.total;
+  if (w.split) {
+    const size_t slots = (size_t)d->num_seqs * nseg_max * d->num_kv_heads;
+    w.seq_split_base = w.total;
+    w.part_o = align_up(w.seq_split_base + seq_ints * 4, 256);
+    w.part_lse = align_up(w.part_o + slots * ppa::kRowsPerTile * d->head_dim * 4, 256);
+    w.total = align_up(w.part_lse + slots * ppa::kRowsPerTile * 4, 256);
+  }
   w.has_row_bounds = d->max_mm_ranges > 0;
   w.row_bounds = w.total;
   if (w.has_row_bounds) w.total = align_up(w.row_bounds + (size_t)d->total_q * 8, 256);
@@ -174,6 +199,7 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   const long long mq = max_qtiles_for(dims, tq);
   if (mq * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
   const WsLayout w = ws_layout(dims);
+  if (w.max_units * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
   char* ws = static_cast<char*>(workspace);
   ppa::Stage1Params s1{};
   s1.num_seqs = dims->num_seqs;
@@ -197,6 +223,9 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   s1.seq_item_base = reinterpret_cast<int32_t*>(ws + w.seq_item_base);
   s1.units = reinterpret_cast<ppa::Unit*>(ws + w.units);
   s1.items = reinterpret_cast<int32_t*>(ws + w.items);
+  s1.split_tiles = w.split ? dims->kv_split_tiles : 0;
+  s1.max_units = (int)w.max_units;
+  s1.seq_split_base = w.split ? reinterpret_cast<int32_t*>(ws + w.seq_split_base) : nullptr;
   s1.bounds_out = nullptr;
   s1.status = device_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -235,6 +264,7 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   const long long mq = max_qtiles_for(dims, tq);
   if (mq * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
   const WsLayout w = ws_layout(dims);
+  if (w.max_units * dims->num_kv_heads > INT_MAX) return PPA_ERR_INVALID;
   char* ws = static_cast<char*>(workspace);
 
   ppa::AttnParams a{};
@@ -253,6 +283,8 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.units = reinterpret_cast<const ppa::Unit*>(ws + w.units);
   a.items = reinterpret_cast<const int32_t*>(ws + w.items);
   a.row_bounds = w.has_row_bounds ? reinterpret_cast<const int32_t*>(ws + w.row_bounds) : nullptr;
+  a.part_o = w.split ? reinterpret_cast<float*>(ws + w.part_o) : nullptr;
+  a.part_lse = w.split ? reinterpret_cast<float*>(ws + w.part_lse) : nullptr;
   a.status = device_status;
   a.kv_in_cache = in_cache ? 1 : 0;
   a.mask = mask_of(dims, mm_ranges);
@@ -272,7 +304,7 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
     ppa::Fp8DequantParams f{};
     f.ws = a.ws;
     f.units = a.units;
-    f.max_units = (int)mq;
+    f.max_units = (int)w.max_units;
     f.context_lens = context_lens;
     f.block_table = block_table;
     f.k_cache = k_cache;
@@ -319,12 +351,26 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   if (!maps_ok) return PPA_ERR_CUDA;
   const float sm = dims->sm_scale > 0.f ? dims->sm_scale : 1.0f / std::sqrt((float)dims->head_dim);
   a.scale_log2 = sm * 1.4426950408889634f;
-  const int max_items = (int)(mq * dims->num_kv_heads);
+  const int max_items = (int)(w.max_units * dims->num_kv_heads);
   cudaError_t e;
   switch (dims->head_dim) {
     case 64: e = ppa::launch_attn_d64(a, fp8_kernel, max_items, s); break;
     case 128: e = ppa::launch_attn_d128(a, fp8_kernel, max_items, s); break;
     default: e = ppa::launch_attn_d256(a, fp8_kernel, max_items, s); break;
+  }
+  if (e == cudaSuccess && w.split) {  // segments of split sequences -> the output rows
+    ppa::MergeParams m{};
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.seq_split_base = reinterpret_cast<const int32_t*>(ws + w.seq_split_base);
+    m.cu_query_lens = cu_query_lens;
+    m.out = out;
+    m.num_seqs = dims->num_seqs;
+    m.num_kv_heads = dims->num_kv_heads;
+    m.group = G;
+    m.head_dim = D;
+    m.num_q_heads = dims->num_q_heads;
+    e = ppa::launch_split_merge(m, s);
   }
   return e == cudaSuccess ? PPA_OK : PPA_ERR_CUDA;
 }

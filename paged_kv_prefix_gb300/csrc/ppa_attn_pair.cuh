@@ -594,19 +594,23 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
       for (int e = 0; e < 4; ++e)
         dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
     };
-    // 32-column chunks, the load of the next in flight while one is converted and stored
-    static_assert((D / 32) % 2 == 0, "chunk pairs");
-    uint32_t oa[32], ob[32];
-    tmem_ld_32_async(tO, oa);
-    tmem_ld_wait(oa);
+    if (u.part >= 0) {  // a split-KV segment: O / l in fp32 and the row's log-sum-exp
+      split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
+    } else {
+      // 32-column chunks, the load of the next in flight while one is converted and stored
+      static_assert((D / 32) % 2 == 0, "chunk pairs");
+      uint32_t oa[32], ob[32];
+      tmem_ld_32_async(tO, oa);
+      tmem_ld_wait(oa);
 #pragma unroll 1
-    for (int cc = 0; cc < D / 32; cc += 2) {
-      tmem_ld_32_async(tO + (cc + 1) * 32, ob);
-      store32(oa, cc);
-      tmem_ld_wait(ob);
-      if (cc + 2 < D / 32) tmem_ld_32_async(tO + (cc + 2) * 32, oa);
-      store32(ob, cc + 1);
-      if (cc + 2 < D / 32) tmem_ld_wait(oa);
+      for (int cc = 0; cc < D / 32; cc += 2) {
+        tmem_ld_32_async(tO + (cc + 1) * 32, ob);
+        store32(oa, cc);
+        tmem_ld_wait(ob);
+        if (cc + 2 < D / 32) tmem_ld_32_async(tO + (cc + 2) * 32, oa);
+        store32(ob, cc + 1);
+        if (cc + 2 < D / 32) tmem_ld_wait(oa);
+      }
     }
     tc_fence_before();
     __syncwarp();

@@ -152,6 +152,7 @@ __device__ __forceinline__ void ring_put(const WsShared& sh, const AttnParams& p
 struct UnitInfo {
   int b, g, t0, nt, c, n, s, q_start, lo, hi;
   int cs;  // key positions below cs come from the cache: c, or s when K/V are in the cache
+  int part;  // split-KV segment: partial-result slot, -1 when the unit writes the output
   int lo_i[2], hi_i[2];
 };
 
@@ -168,6 +169,7 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   u.n = p.cu_query_lens[u.b + 1] - u.q_start;
   u.s = u.c + u.n;
   u.cs = p.kv_in_cache ? u.s : u.c;
+  u.part = un.part;
   u.lo_i[0] = un.lo0;
   u.hi_i[0] = un.hi0;
   u.lo_i[1] = un.nt > 1 ? un.lo1 : 0;
@@ -673,6 +675,35 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
 // ---------------------------------------------------------------------------------------
 // Softmax role (warps 0-7): warpgroup i owns query tile i; thread r owns row r.
 // ---------------------------------------------------------------------------------------
+// Split-KV epilogue of one row (thread `r` of a query tile): O / l as D fp32 values and the
+// row's base-2 log-sum-exp over this segment's keys, m + log2(l) with m the exp2 reference the
+// row's P used (-inf when none of the segment's keys is allowed), into partial slot
+// u.part * Hkv + u.g. The merge kernel combines a sequence's segments.
+template <int D>
+__device__ __forceinline__ void split_partial_store(const AttnParams& p, const UnitInfo& u, int r,
+                                                    bool row_valid, float m_ref, float l_run,
+                                                    float inv_l, uint32_t tO) {
+  const size_t slot = (size_t)u.part * p.num_kv_heads + u.g;
+  float* orow = p.part_o + (slot * kRowsPerTile + r) * D;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t o32[32];
+    tmem_ld_32(tO + cc * 32, o32);
+    if (row_valid) {
+      float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(o32[4 * e]) * inv_l, __uint_as_float(o32[4 * e + 1]) * inv_l,
+                             __uint_as_float(o32[4 * e + 2]) * inv_l, __uint_as_float(o32[4 * e + 3]) * inv_l);
+    }
+  }
+  if (row_valid) {
+    const float neg_inf = -__int_as_float(0x7f800000);
+    const float m_use = m_ref == neg_inf ? 0.f : m_ref;
+    p.part_lse[slot * kRowsPerTile + r] = l_run > 0.f ? m_use + log2f(l_run) : neg_inf;
+  }
+}
+
 template <int D, bool FP8>
 __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tmem) {
   using C = WsCfg<D>;
@@ -814,6 +845,12 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     od_phase ^= 1;
     tc_fence_after();
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+    if (u.part >= 0) {  // a split-KV segment: O / l in fp32 and the row's base-2 log-sum-exp
+      split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
+      tc_fence_before();
+      mbar_arrive(sh.bar(wsbar::O_EMPTY + 8 * i));
+      continue;
+    }
     __nv_bfloat16* orow =
         static_cast<__nv_bfloat16*>(p.out) +
         ((size_t)(u.q_start + (row_valid ? j : 0)) * p.num_q_heads + u.g * p.group + hh) * D;

@@ -53,6 +53,7 @@ struct WsHeader {
 // key tiles in the union.
 struct Unit {
   int32_t seq, t0, nt, lo0, hi0, lo1, hi1, cost;
+  int32_t part;  // split-KV segment: its partial-result slot (x Hkv + kv head); -1: not split
 };
 
 __device__ __forceinline__ void report(int32_t* status, int code) {

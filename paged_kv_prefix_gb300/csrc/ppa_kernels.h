@@ -25,8 +25,12 @@ struct Stage1Params {
   int32_t* seq_cost;       // [B]     key tiles summed over the sequence's units
   int32_t* seq_order;      // [B]     sequences, heaviest first
   int32_t* seq_item_base;  // [B + 1] first item of each sequence in heaviest-first order
-  Unit* units;             // [max_qtiles]
-  int32_t* items;          // [max_qtiles * num_kv_heads]: unit * Hkv + kv head
+  Unit* units;             // [max_units]
+  int32_t* items;          // [max_units * num_kv_heads]: unit * Hkv + kv head
+  // split-KV: a sequence with one query tile becomes segments of split_tiles key tiles
+  int split_tiles;         // 0: off
+  int max_units;           // capacity of units / items
+  int32_t* seq_split_base; // [B + 1] first partial slot of each split sequence (or nullptr)
   // bounds-only mode
   int32_t* bounds_out;     // [max_qtiles][2]
   int32_t* status;
@@ -64,6 +68,10 @@ struct AttnParams {
   const int32_t* row_bounds;  // [total_q][2] row intervals when multimodal ranges are given
   int32_t* status;
   int kv_in_cache;  // new tokens' K/V read from the cache (positions c .. s-1); k_new unused
+  // split-KV partial results: slot (part * Hkv + g) holds 128 rows of D fp32 (O / l) and 128
+  // base-2 log-sum-exps
+  float* part_o;
+  float* part_lse;
   MaskParams mask;
   int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
   float scale_log2;  // softmax scale * log2(e)
@@ -130,6 +138,18 @@ struct AppendParams {
   int fp8;
 };
 cudaError_t launch_append_kv(const AppendParams& p, cudaStream_t stream);
+
+// Split-KV merge (ppa_stage1.cu): for every split sequence and KV head, the segments' partial
+// rows combined by their log-sum-exps into the bf16 output.
+struct MergeParams {
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* seq_split_base;  // [B + 1]
+  const int32_t* cu_query_lens;
+  void* out;  // bf16 [total_q][Hq][D]
+  int num_seqs, num_kv_heads, group, head_dim, num_q_heads;
+};
+cudaError_t launch_split_merge(const MergeParams& p, cudaStream_t stream);
 
 // Attention kernels, one translation unit per head dimension. `max_ctas` bounds the
 // persistent grid (the number of work items cannot be known on the host).

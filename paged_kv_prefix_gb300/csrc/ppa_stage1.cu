@@ -7,6 +7,7 @@
 // "[Kernel][Gemma4] Prune Triton sliding-window tiles for multimodal prefixes" (PR #53147),
 // 实现拆解 2 and 关键源码片段 (compute_tile_loop_bounds: union of the base window and every
 // intersecting multimodal range, clipped to seq_len - 1, converted with // TILE_SIZE).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -160,11 +161,13 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
   if (tid == 0) s_err = 0;
   __syncthreads();
 
-  // 1. units per sequence
-  int carry = 0;
+  // 1. units per sequence. With split-KV, a sequence of one query tile whose live key
+  //    interval spans more than split_tiles key tiles becomes one unit per segment of
+  //    split_tiles key tiles, each with its own partial-result slot.
+  int carry = 0, split_carry = 0;
   for (int b0 = 0; b0 < B; b0 += kStage1Threads) {
     const int b = b0 + tid;
-    int nu = 0;
+    int nu = 0, nseg = 0;
     if (b < B) {
       bool bad = false;
       int c;
@@ -172,17 +175,31 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
       if (bad) atomicExch(&s_err, 1);
       const int nt = (n + p.tq - 1) / p.tq;
       nu = (nt + p.nq - 1) / p.nq;
+      if (p.split_tiles > 0 && nt == 1 && !bad) {
+        int lo, hi;
+        qtile_bounds(p, b, c, n, 0, &lo, &hi);
+        const int segs = (hi - lo + p.split_tiles - 1) / p.split_tiles;
+        if (segs >= 2) nu = nseg = segs;
+      }
       p.seq_cost[b] = 0;
     }
-    int total;
+    int total, stotal;
     const int excl = block_exclusive_scan(nu, s_warp, &total);
     if (b < B) p.seq_unit_base[b] = carry + excl;
     carry += total;
+    if (p.seq_split_base != nullptr) {
+      const int sexcl = block_exclusive_scan(nseg, s_warp, &stotal);
+      if (b < B) p.seq_split_base[b] = split_carry + sexcl;
+      split_carry += stotal;
+    }
   }
   const int n_units = carry;
-  if (tid == 0) p.seq_unit_base[B] = n_units;
+  if (tid == 0) {
+    p.seq_unit_base[B] = n_units;
+    if (p.seq_split_base != nullptr) p.seq_split_base[B] = split_carry;
+  }
   __syncthreads();
-  if (s_err || n_units > p.max_qtiles || (long long)n_units * p.num_kv_heads > INT_MAX) {
+  if (s_err || n_units > p.max_units || (long long)n_units * p.num_kv_heads > INT_MAX) {
     if (tid == 0) {
       report(p.status, PPA_ERR_INVALID);
       p.ws->n_items = 0;
@@ -199,10 +216,18 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
     const int c = p.context_lens[b];
     const int n = p.cu_query_lens[b + 1] - p.cu_query_lens[b];
     const int nt = (n + p.tq - 1) / p.tq;
-    const int t0 = (u - p.seq_unit_base[b]) * p.nq;
-    const int cnt = min(p.nq, nt - t0);
-    Unit un{b, t0, cnt, 0, 0, 0, 0, 0};
+    const int lu = u - p.seq_unit_base[b];
+    const bool split =
+        p.seq_split_base != nullptr && p.seq_split_base[b + 1] > p.seq_split_base[b];
+    const int t0 = split ? 0 : lu * p.nq;
+    const int cnt = split ? 1 : min(p.nq, nt - t0);
+    Unit un{b, t0, cnt, 0, 0, 0, 0, 0, -1};
     qtile_bounds(p, b, c, n, t0, &un.lo0, &un.hi0);
+    if (split) {  // segment lu of the tile's key tiles
+      un.lo0 += lu * p.split_tiles;
+      un.hi0 = min(un.hi0, un.lo0 + p.split_tiles);
+      un.part = p.seq_split_base[b] + lu;
+    }
     int lo = un.lo0, hi = un.hi0;
     if (cnt > 1) {
       qtile_bounds(p, b, c, n, t0 + 1, &un.lo1, &un.hi1);
@@ -430,6 +455,44 @@ cudaError_t launch_row_bounds(const MaskParams& mp, int num_seqs, int total_q, c
   const int blocks = (total_q + 255) / 256;
   row_bounds_kernel<<<blocks < 4096 ? blocks : 4096, 256, 0, stream>>>(mp, num_seqs, total_q, cu,
                                                                        ctx, out);
+  return cudaGetLastError();
+}
+
+// Split-KV merge: one CTA per (sequence, KV head), threads over the head dimension. For each
+// of the tile's rows, the segments' rows O_s (already divided by their own row sums) weigh in
+// with 2^(lse_s - max lse): softmax over the union of the segments' keys, exactly.
+__global__ void split_merge_kernel(const MergeParams p) {
+  const int b = blockIdx.x / p.num_kv_heads;
+  const int g = blockIdx.x - b * p.num_kv_heads;
+  const int s0 = p.seq_split_base[b], ns = p.seq_split_base[b + 1] - s0;
+  if (ns <= 0) return;
+  const int q0 = p.cu_query_lens[b];
+  const int rows = (p.cu_query_lens[b + 1] - q0) * p.group;  // <= kRowsPerTile
+  for (int r = 0; r < rows; ++r) {
+    float mx = -__int_as_float(0x7f800000);
+    for (int s = 0; s < ns; ++s)
+      mx = fmaxf(mx, p.part_lse[((size_t)(s0 + s) * p.num_kv_heads + g) * kRowsPerTile + r]);
+    const int tok = r / p.group, hh = r - tok * p.group;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                          ((size_t)(q0 + tok) * p.num_q_heads + g * p.group + hh) * p.head_dim;
+    for (int col = threadIdx.x; col < p.head_dim; col += blockDim.x) {
+      float num = 0.f, den = 0.f;
+      for (int s = 0; s < ns; ++s) {
+        const size_t slot = (size_t)(s0 + s) * p.num_kv_heads + g;
+        const float lse = p.part_lse[slot * kRowsPerTile + r];
+        if (lse == -__int_as_float(0x7f800000)) continue;  // no keys of the row in segment s
+        const float w = exp2f(lse - mx);
+        den += w;
+        num += w * p.part_o[(slot * kRowsPerTile + r) * p.head_dim + col];
+      }
+      orow[col] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+    }
+  }
+}
+
+cudaError_t launch_split_merge(const MergeParams& p, cudaStream_t stream) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  split_merge_kernel<<<p.num_seqs * p.num_kv_heads, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -346,6 +346,16 @@ def chunked_local(seed: int = 0, scale: float = 1.0, num_seqs: int = 4, seq_len:
                       544, causal=True, chunk_size=c, chunk_lookback=lookback, seed=seed, **kw)
 
 
+def decode(seed: int = 0, scale: float = 1.0, num_seqs: int = 32, new_tokens: int = 1,
+           **kw) -> PrefillCase:
+    """Decode over long contexts: 32 sequences, context U[8192, 32768], 1 new token each
+    (``new_tokens`` > 1: speculative verification), 32 q / 8 kv heads, D 128, page 544, causal."""
+    rng = np.random.default_rng([seed, 404])
+    ctx = [_scaled(int(x), scale) for x in rng.integers(8192, 32769, size=num_seqs)]
+    return build_case(f"decode_n{new_tokens}", ctx, [new_tokens] * num_seqs, 32, 8, 128, 544,
+                      causal=True, seed=seed, **kw)
+
+
 def mm_ranges_for(seq_len: int, num_ranges: int, width: int, rng: np.random.Generator) -> np.ndarray:
     """Non-overlapping ranges [a, a + width - 1] at seeded random starts."""
     free = seq_len - num_ranges * width
