@@ -186,8 +186,9 @@ ppa_status ppa_append_kv(const ppa_dims* dims, const void* k_new, const void* v_
                          void* stream);
 
 /* Size of the scratch ppa_prefill_noalloc keeps in a static device array: 2 MiB. The scratch a
- * batch needs is ppa_workspace_bytes(): about 32 + 4 * num_kv_heads bytes per query tile plus 16
- * bytes per sequence, so 2 MiB holds, for example, about 32,000 query tiles at 8 KV heads. */
+ * batch needs is ppa_workspace_bytes(): about 36 + 4 * num_kv_heads bytes per query tile plus 16
+ * bytes per sequence, so 2 MiB holds, for example, about 30,000 query tiles at 8 KV heads
+ * (more with multimodal ranges or split-KV, whose extra scratch counts too). */
 #define PPA_NOALLOC_WORKSPACE_BYTES (2u << 20)
 
 /* ppa_prefill for callers that cannot allocate device memory: no workspace argument.
