@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached|chunked|
                                 decode|decode_split] [--no-cpu-baseline]
-                    [--sweep windows]
+                    [--sweep windows|pages]
 
 A step is one pass of the whole hot path over one batch: for every shape of the workload,
 stage 1 (live key-tile bounds and work list) and the attention kernel, through the C ABI.
@@ -615,6 +615,48 @@ def run_window_sweep(args):
             del dc
 
 
+def run_page_sweep(args):
+    """One ragged batch (8 sequences, context U[0, 8192], 1-2048 new tokens, causal) at every
+    page size the pages name and each head shape: with key tiles that straddle pages, the
+    throughput should not depend on the page size. One JSON line per point."""
+    import torch
+    from paged_kv_prefix_gb300 import binding
+    from paged_kv_prefix_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(0)
+    ctx = rng.integers(0, 8193, size=8)
+    qlen = rng.integers(1, 2049, size=8)
+    for hq, hkv, d in ((64, 64, 128), (32, 8, 128), (8, 2, 256), (16, 16, 64)):
+        for page in (16, 128, 512, 544, 1040, 1056, 2048):
+            case = wl.build_case(f"pages_h{hq}_g{hq // hkv}_d{d}_p{page}", ctx, qlen, hq, hkv, d,
+                                 page, causal=True, seed=0)
+            dc = binding.DeviceCase(case)
+            flops = algorithmic_flops(binding, dc, case, stream)
+            nbytes = algorithmic_bytes(binding, dc, case, stream)
+            dc.plan(stream)
+            ms = []
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dc.attend(stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if k >= args.warmup:
+                    ms.append(e0.elapsed_time(e1))
+            st = dc.read_status(stream)
+            t = float(np.median(ms)) * 1e-3
+            print(json.dumps({"sweep": "page_size", "num_q_heads": hq, "group": hq // hkv,
+                              "head_dim": d, "page_size": page, "attend_ms": t * 1e3,
+                              "tflops": flops / t / 1e12, "gbs": nbytes / t / 1e9,
+                              "roofline": roofline(flops, nbytes, t, peaks, peak_src),
+                              "status": st}), flush=True)
+            del dc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -625,13 +667,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
-    ap.add_argument("--sweep", choices=["windows"], default=None,
+    ap.add_argument("--sweep", choices=["windows", "pages"], default=None,
                     help="print one line per point of a window / length sweep instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.sweep == "windows":
         run_window_sweep(args)
+    elif args.sweep == "pages":
+        run_page_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
