@@ -354,9 +354,9 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   const int max_items = (int)(w.max_units * dims->num_kv_heads);
   cudaError_t e;
   switch (dims->head_dim) {
-    case 64: e = ppa::launch_attn_d64(a, fp8_kernel, max_items, s); break;
-    case 128: e = ppa::launch_attn_d128(a, fp8_kernel, max_items, s); break;
-    default: e = ppa::launch_attn_d256(a, fp8_kernel, max_items, s); break;
+    case 64: e = ppa::launch_attn_d64(a, fp8_kernel, w.split, max_items, s); break;
+    case 128: e = ppa::launch_attn_d128(a, fp8_kernel, w.split, max_items, s); break;
+    default: e = ppa::launch_attn_d256(a, fp8_kernel, w.split, max_items, s); break;
   }
   if (e == cudaSuccess && w.split) {  // segments of split sequences -> the output rows
     ppa::MergeParams m{};

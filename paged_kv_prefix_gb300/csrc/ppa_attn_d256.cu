@@ -4,9 +4,13 @@
 
 namespace ppa {
 
-cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream) {
-  return fp8 ? launch_attn_pair<256, true>(p, max_items, stream)
-             : launch_attn_pair<256, false>(p, max_items, stream);
+cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, bool split, int max_items,
+                             cudaStream_t stream) {
+  if (split)  // the split-KV epilogue is compiled only into these instances
+    return fp8 ? launch_attn_pair<256, true, true>(p, max_items, stream)
+               : launch_attn_pair<256, false, true>(p, max_items, stream);
+  return fp8 ? launch_attn_pair<256, true, false>(p, max_items, stream)
+             : launch_attn_pair<256, false, false>(p, max_items, stream);
 }
 
 }  // namespace ppa

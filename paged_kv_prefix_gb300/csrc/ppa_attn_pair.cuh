@@ -437,7 +437,7 @@ __device__ void pair_mma(const AttnParams& p, const PairShared& sh, uint32_t bas
 // ---------------------------------------------------------------------------------------
 // Softmax (warps 0-3 of each CTA): thread r owns row r of this CTA's query tile.
 // ---------------------------------------------------------------------------------------
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t tmem) {
   using C = PairCfg<D>;
   const int warp = threadIdx.x >> 5;
@@ -594,8 +594,8 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
       for (int e = 0; e < 4; ++e)
         dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
     };
-    if (u.part >= 0) {  // a split-KV segment: O / l in fp32 and the row's log-sum-exp
-      split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
+    if (SPLIT && u.part >= 0) {  // a split-KV segment: O / l in fp32 and its log-sum-exp
+      if constexpr (SPLIT) split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
     } else {
       // 32-column chunks, the load of the next in flight while one is converted and stored
       static_assert((D / 32) % 2 == 0, "chunk pairs");
@@ -620,7 +620,7 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
     attn_pair_kernel(const __grid_constant__ AttnParams p) {
   using C = PairCfg<D>;
@@ -676,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   // 384 threads x 168 registers at launch: softmax warpgroup 232, the other two 136 each.
   if (warp < 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
-    pair_softmax<D, FP8>(p, sh, tmem);
+    pair_softmax<D, FP8, SPLIT>(p, sh, tmem);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 136;\n" ::: "memory");
   }
@@ -721,7 +721,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 cudaError_t launch_attn_pair(const AttnParams& p, int max_items, cudaStream_t stream) {
   using C = PairCfg<D>;
   int dev = 0;
@@ -731,7 +731,7 @@ cudaError_t launch_attn_pair(const AttnParams& p, int max_items, cudaStream_t st
   static int sm_count[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_pair_kernel<D, FP8>,
+    e = cudaFuncSetAttribute(attn_pair_kernel<D, FP8, SPLIT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -739,7 +739,7 @@ cudaError_t launch_attn_pair(const AttnParams& p, int max_items, cudaStream_t st
     configured[dev] = 1;
   }
   const int pairs = max(1, min(sm_count[dev] / 2, max_items));
-  attn_pair_kernel<D, FP8><<<2 * pairs, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_pair_kernel<D, FP8, SPLIT><<<2 * pairs, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 

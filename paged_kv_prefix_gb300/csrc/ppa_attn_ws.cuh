@@ -704,7 +704,7 @@ __device__ __forceinline__ void split_partial_store(const AttnParams& p, const U
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tmem) {
   using C = WsCfg<D>;
   const int warp = threadIdx.x >> 5;
@@ -845,11 +845,13 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
     od_phase ^= 1;
     tc_fence_after();
     const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-    if (u.part >= 0) {  // a split-KV segment: O / l in fp32 and the row's base-2 log-sum-exp
-      split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
-      tc_fence_before();
-      mbar_arrive(sh.bar(wsbar::O_EMPTY + 8 * i));
-      continue;
+    if constexpr (SPLIT) {  // only launches with split-KV carry this path
+      if (u.part >= 0) {  // a split-KV segment: O / l in fp32 and the row's log-sum-exp
+        split_partial_store<D>(p, u, r, row_valid, m_ref, l_run, inv_l, tO);
+        tc_fence_before();
+        mbar_arrive(sh.bar(wsbar::O_EMPTY + 8 * i));
+        continue;
+      }
     }
     __nv_bfloat16* orow =
         static_cast<__nv_bfloat16*>(p.out) +
@@ -874,7 +876,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__ AttnParams p) {
   using C = WsCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -932,7 +934,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
 
   if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
-    ws_softmax<D, FP8>(p, sh, tmem);
+    ws_softmax<D, FP8, SPLIT>(p, sh, tmem);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp < 12) {
@@ -970,7 +972,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPLIT>
 cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stream) {
   using C = WsCfg<D, FP8>;
   int dev = 0;
@@ -980,7 +982,7 @@ cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stre
   static int sm_count[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_ws_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_ws_kernel<D, FP8, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -988,7 +990,7 @@ cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stre
     configured[dev] = 1;
   }
   const int grid = max(1, min(sm_count[dev], max_items));
-  attn_ws_kernel<D, FP8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  attn_ws_kernel<D, FP8, SPLIT><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -153,8 +153,11 @@ cudaError_t launch_split_merge(const MergeParams& p, cudaStream_t stream);
 
 // Attention kernels, one translation unit per head dimension. `max_ctas` bounds the
 // persistent grid (the number of work items cannot be known on the host).
-cudaError_t launch_attn_d64(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
-cudaError_t launch_attn_d128(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
-cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, int max_items, cudaStream_t stream);
+cudaError_t launch_attn_d64(const AttnParams& p, bool fp8, bool split, int max_items,
+                             cudaStream_t stream);
+cudaError_t launch_attn_d128(const AttnParams& p, bool fp8, bool split, int max_items,
+                             cudaStream_t stream);
+cudaError_t launch_attn_d256(const AttnParams& p, bool fp8, bool split, int max_items,
+                             cudaStream_t stream);
 
 }  // namespace ppa
