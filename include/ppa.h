@@ -199,8 +199,12 @@ ppa_status ppa_append_kv(const ppa_dims* dims, const void* k_new, const void* v_
  * instead in one file-scope device array of PPA_NOALLOC_WORKSPACE_BYTES, which every GPU that
  * loads the library holds until the process exits. This call allocates and frees nothing.
  *   - Inputs, `out` and `device_status` are the caller's, exactly as for ppa_prefill.
- *   - A batch whose ppa_workspace_bytes() exceeds PPA_NOALLOC_WORKSPACE_BYTES is rejected
- *     with PPA_ERR_UNSUPPORTED before anything is launched (use ppa_prefill for it).
+ *   - fp8 caches are widened inside the attention kernel (as with PPA_FLAG_FP8_INKERNEL)
+ *     and kv_split_tiles is ignored: the dequantisation staging and the split partials do
+ *     not fit the fixed scratch. The output is the same attention either way.
+ *   - A batch whose ppa_workspace_bytes() (for those settings) exceeds
+ *     PPA_NOALLOC_WORKSPACE_BYTES is rejected with PPA_ERR_UNSUPPORTED before anything is
+ *     launched (use ppa_prefill for it).
  *   - The first call on each device looks up that device's address of the array (with the
  *     device current) and caches it; make that first call before any stream capture.
  *   - All calls on a device share the one array. Calls whose work overlaps on the GPU (other

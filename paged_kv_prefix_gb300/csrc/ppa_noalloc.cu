@@ -50,10 +50,12 @@ extern "C" ppa_status ppa_prefill_noalloc(const ppa_dims* dims, const void* q, c
                                           const float* k_scale, const float* v_scale, void* out,
                                           int32_t* device_status, void* stream) {
   if (dims == nullptr) return PPA_ERR_INVALID;
-  // fp8 caches widen inside the attention kernel here: the bf16 staging of the live cache
-  // tiles would not fit the fixed scratch.
+  // fp8 caches widen inside the attention kernel here, and split-KV is off: neither the bf16
+  // staging of the live cache tiles nor the split partials would fit the fixed scratch. Both
+  // change only how the result is computed, not the result.
   ppa_dims d = *dims;
   if (d.kv_dtype == PPA_KV_FP8_E4M3) d.flags |= PPA_FLAG_FP8_INKERNEL;
+  d.kv_split_tiles = 0;
   dims = &d;
   const size_t need = ppa_workspace_bytes(dims);
   if (need == 0) {

@@ -43,6 +43,21 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         assert_close(out.float().cpu().numpy(), want, f"noalloc {case.name}")
 
 
+def test_noalloc_runs_split_kv_batches_unsplit():
+    """kv_split_tiles does not fit the fixed scratch: the batch runs unsplit, same output."""
+    case = wl.build_case("noalloc_split", [3000, 200], [1, 4], 8, 2, 128, 37, causal=True,
+                         seed=34)
+    dc = binding.DeviceCase(case, kv_split_tiles=4)
+    dc.run()
+    torch.cuda.synchronize()
+    assert dc.read_status() == binding.PPA_OK
+    out = torch.full_like(dc.out, float("nan"))
+    assert _noalloc(dc, out) == binding.PPA_OK
+    torch.cuda.synchronize()
+    assert dc.read_status() == binding.PPA_OK
+    assert_close(out.float().cpu().numpy(), dc.out.float().cpu().numpy(), "noalloc split")
+
+
 def test_noalloc_rejects_a_batch_larger_than_its_scratch():
     case = wl.tiny()
     dc = binding.DeviceCase(case)
