@@ -74,6 +74,8 @@ def test_fp8_workspace_holds_the_bf16_staging_unless_widened_in_kernel():
     ("flags", 64, binding.PPA_ERR_INVALID),
     ("sm_scale", float("nan"), binding.PPA_ERR_INVALID),
     ("max_mm_ranges", -2, binding.PPA_ERR_INVALID),
+    ("chunk_size", -1, binding.PPA_ERR_INVALID),
+    ("kv_split_tiles", -3, binding.PPA_ERR_INVALID),
 ])
 def test_invalid_dims_rejected(field, value, code):
     d = _dims(**{field: value})
@@ -83,11 +85,53 @@ def test_invalid_dims_rejected(field, value, code):
     assert got == code
 
 
+def test_chunk_lookback_must_be_non_negative_with_chunks():
+    f = 1 << 20
+    args = [f] * 8 + [None, None, None, f, f, f]
+    d = _dims(chunk_size=16, chunk_lookback=-1)
+    assert binding.ppa_prefill(d, *args, stream=0, check=False) == binding.PPA_ERR_INVALID
+    assert binding.ppa_workspace_bytes(d) == 0
+    assert binding.ppa_workspace_bytes(_dims(chunk_size=16, chunk_lookback=2)) > 0
+    # without chunks the lookback is ignored
+    assert binding.ppa_workspace_bytes(_dims(chunk_size=0, chunk_lookback=-1)) > 0
+
+
+def test_split_kv_workspace_holds_the_partials():
+    base = _dims()
+    split = _dims(kv_split_tiles=4)
+    extra = binding.ppa_workspace_bytes(split) - binding.ppa_workspace_bytes(base)
+    tq = 128 // (base.num_q_heads // base.num_kv_heads)
+    tiles = -(-(base.max_pages_per_seq * base.page_size + tq) // 128)
+    nseg = -(-tiles // 4)
+    slots = base.num_seqs * nseg * base.num_kv_heads
+    partials = slots * 128 * (base.head_dim + 1) * 4  # O rows and log-sum-exps, fp32
+    assert partials <= extra <= partials + 4 * 256 + base.num_seqs * (nseg - 1) * (
+        36 + 4 * base.num_kv_heads) + 8 * (base.num_seqs + 1)
+
+
+def test_append_kv_validates_on_the_host():
+    d = _dims()
+    f = 1 << 20
+    # every call below is rejected (or has no work) before anything is launched
+    ok = [f, f, f, f, f, f, f, None, None, f]  # k_new .. context_lens, scales, status
+    for i, name in [(0, "k_new"), (2, "k_cache"), (4, "block_table"), (9, "status")]:
+        a = list(ok)
+        a[i] = None
+        assert binding.ppa_append_kv(d, *a, stream=0, check=False) == binding.PPA_ERR_INVALID, name
+    a = list(ok)
+    a[1] = f + 8  # misaligned v_new
+    assert binding.ppa_append_kv(d, *a, stream=0, check=False) == binding.PPA_ERR_INVALID
+    d8 = _dims(kv_dtype=binding.PPA_KV_FP8_E4M3)  # fp8 without scales
+    assert binding.ppa_append_kv(d8, *ok, stream=0, check=False) == binding.PPA_ERR_INVALID
+    empty = _dims(num_seqs=0, total_q=0)
+    assert binding.ppa_append_kv(empty, *ok, stream=0, check=False) == binding.PPA_OK
+
+
 def test_null_and_misaligned_pointers_rejected():
     d = _dims()
     f = 1 << 20
     args = [f] * 8 + [None, None, None, f, f, f]  # never launched: each call below is rejected
-    # cache-sourced path (k_new = NULL) is not available
+    # k_new = NULL needs PPA_FLAG_KV_IN_CACHE
     a = list(args)
     a[1] = None
     assert binding.ppa_prefill(d, *a, stream=0, check=False) == binding.PPA_ERR_UNSUPPORTED
