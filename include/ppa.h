@@ -5,14 +5,17 @@
  * tokens and n = cu_query_lens[b+1] - cu_query_lens[b] new query tokens, so s = c + n keys.
  * Query token j of sequence b sits at absolute position q = c + j. Key positions p < c are
  * read from the paged cache through the block table, one token at a time: physical page
- * block_table[b][p / P], slot p % P. Key positions p >= c are read from k_new / v_new.
+ * block_table[b][p / P], slot p % P. Key positions p >= c are read from k_new / v_new, or,
+ * with PPA_FLAG_KV_IN_CACHE, from the cache as well (after ppa_append_kv wrote them there).
  * Tiles of keys may therefore straddle page boundaries, and P may be any positive integer.
  * Sources: vLLM PR #54194 report (prefix-prefill tiles decoupled from the page size),
  * sections "功能与动机" and "关键源码片段" (context_attention_fwd, _paged_kv_cache_offsets).
  *
  * Mask: a query at q may attend to key k (0 <= k < s) iff base(q,k) OR mm(q,k).
  *   base: (causal ? k <= q : (window_right <= 0 || k - q < window_right))
- *         && (window_left <= 0 || q - k < window_left)
+ *         && (chunk_size > 0 ? k >= ((q / chunk_size) - chunk_lookback) * chunk_size
+ *                            : (window_left <= 0 || q - k < window_left))
+ *         with `causal` per sequence when ppa_dims.seq_causal is given
  *   mm:   some range [a, e] of the sequence with a < e has a <= q <= e' and a <= k <= e',
  *         with e' = min(e, s - 1), and, when PPA_FLAG_CLAMP_MM is set and window_left > 0,
  *         also q - k < window_left.
@@ -38,7 +41,8 @@
  *   mm_ranges    [num_seqs][max_mm_ranges][2]                int32 {start, end}, end inclusive;
  *                                                            entries with start >= end are unused
  *   out          [total_q][num_q_heads][head_dim]            bf16
- * Only the first ceil(c / P) entries of a block-table row are ever read.
+ * Only the first ceil(c / P) entries of a block-table row are ever read (ceil((c + n) / P)
+ * with PPA_FLAG_KV_IN_CACHE, and by ppa_append_kv).
  *
  * Ownership and synchronisation: every pointer is a device pointer owned by the caller.
  * The library allocates nothing, never frees, never synchronises inside ppa_prefill, and
