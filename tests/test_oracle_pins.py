@@ -539,3 +539,74 @@ def test_per_sequence_causal_flags_select_each_sequences_mask():
     rows = [(0, 15, all_c), (15, 24, all_n), (24, 35, all_c)]
     for a, e, want in rows:
         assert np.array_equal(out[a:e], want[a:e])
+
+
+@pytest.mark.parametrize("chunk,lookback", [(4, 0), (8, 1), (5, 2)])
+def test_chunked_local_against_torch_sdpa(chunk, lookback):
+    """Chunked-local attention with context and GQA, against torch SDPA fed a block mask built
+    from position indices with integer floor division (k // CS >= q // CS - LB) and K/V
+    expanded per query head."""
+    rng = np.random.default_rng(60 + chunk)
+    c, n, hkv, g, d = 19, 14, 2, 2, 8
+    ctx_k, ctx_v = rng.standard_normal((c, hkv, d)), rng.standard_normal((c, hkv, d))
+    q = rng.standard_normal((n, hkv * g, d))
+    kn, vn = rng.standard_normal((n, hkv, d)), rng.standard_normal((n, hkv, d))
+    inp = _manual_inp(q, kn, vn, ctx_k, ctx_v, causal=True, page_size=7)
+    inp["chunk_size"], inp["chunk_lookback"] = chunk, lookback
+    out = ref.attention(inp, dtype=np.float64)
+    K = torch.from_numpy(np.concatenate([ctx_k, kn])).permute(1, 0, 2).repeat_interleave(g, 0)
+    V = torch.from_numpy(np.concatenate([ctx_v, vn])).permute(1, 0, 2).repeat_interleave(g, 0)
+    Q = torch.from_numpy(q).permute(1, 0, 2)
+    qpos = torch.arange(c, c + n)[:, None]
+    kpos = torch.arange(c + n)[None, :]
+    mask = (kpos <= qpos) & (kpos // chunk >= qpos // chunk - lookback)
+    expect = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask)
+    assert np.allclose(out, expect.permute(1, 0, 2).numpy(), atol=1e-12)
+
+
+def test_per_sequence_causal_against_torch_sdpa():
+    """Two sequences, one causal and one bidirectional with a right window, each against torch
+    SDPA with its own mask."""
+    rng = np.random.default_rng(61)
+    d, hkv, g = 8, 1, 2
+    seqs = [(6, 9, True), (4, 11, False)]
+    qs, kns, vns, out_want = [], [], [], []
+    blocks = []
+    for c, n, causal in seqs:
+        ck, cv = rng.standard_normal((c, hkv, d)), rng.standard_normal((c, hkv, d))
+        q = rng.standard_normal((n, hkv * g, d))
+        kn, vn = rng.standard_normal((n, hkv, d)), rng.standard_normal((n, hkv, d))
+        K = torch.from_numpy(np.concatenate([ck, kn])).permute(1, 0, 2).repeat_interleave(g, 0)
+        V = torch.from_numpy(np.concatenate([cv, vn])).permute(1, 0, 2).repeat_interleave(g, 0)
+        qpos = torch.arange(c, c + n)[:, None]
+        kpos = torch.arange(c + n)[None, :]
+        mask = (kpos <= qpos) if causal else (kpos - qpos < 3)
+        out_want.append(torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q).permute(1, 0, 2), K, V, attn_mask=mask).permute(1, 0, 2).numpy())
+        blocks.append((ck, cv, q, kn, vn))
+    # the batch: both sequences' contexts on contiguous pages of 4
+    P = 4
+    pages = [math.ceil((c + n) / P) for c, n, _ in seqs]
+    kc = np.zeros((sum(pages), P, hkv, d))
+    vc = np.zeros_like(kc)
+    bt = np.zeros((2, max(pages)), dtype=np.int64)
+    base = 0
+    for b, ((c, n, _), (ck, cv, *_)) in enumerate(zip(seqs, blocks)):
+        bt[b, :pages[b]] = np.arange(base, base + pages[b])
+        for p in range(c):
+            kc[base + p // P, p % P], vc[base + p // P, p % P] = ck[p], cv[p]
+        base += pages[b]
+    inp = {
+        "q": np.concatenate([blk[2] for blk in blocks]),
+        "k_new": np.concatenate([blk[3] for blk in blocks]),
+        "v_new": np.concatenate([blk[4] for blk in blocks]),
+        "k_cache": kc, "v_cache": vc, "block_table": bt,
+        "cu_query_lens": np.array([0, 9, 20]), "context_lens": np.array([6, 4]),
+        "mm_ranges": None, "page_size": P, "num_q_heads": hkv * g, "num_kv_heads": hkv,
+        "head_dim": d, "causal": True, "window_left": 0, "window_right": 3, "clamp_mm": False,
+        "sm_scale": 0.0, "kv_dtype": "bf16", "k_scale": 1.0, "v_scale": 1.0,
+        "seq_causal": np.array([True, False]),
+    }
+    out = ref.attention(inp, dtype=np.float64)
+    assert np.allclose(out[:9], out_want[0], atol=1e-12)
+    assert np.allclose(out[9:], out_want[1], atol=1e-12)
