@@ -1,17 +1,19 @@
 """Benchmark: chunked-prefill attention over a paged KV cache on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload nonpow2|swa64|swa1024|mm|mixed|mixed_fp8|mixed_window|mixed_cached|chunked|
-                                decode|decode_split] [--no-cpu-baseline]
-                    [--sweep windows|pages]
+                    [--workload mixed_serving|mixed_serving_fp8|nonpow2|swa64|swa1024|mm|mixed|
+                                mixed_fp8|mixed_window|mixed_cached|chunked|decode|decode_split]
+                    [--no-cpu-baseline] [--sweep windows|pages]
 
-A step is one pass of the whole hot path over one batch: for every shape of the workload,
-stage 1 (live key-tile bounds and work list) and the attention kernel, through the C ABI.
-The default workload is the non-power-of-2-pages batch: 8 ragged sequences (context
-U[0, 8192], query U[1, 2048], causal) for each of the head shapes (64 q heads, G 1, D 128,
-page 544), (8, G 4, D 256, page 1040) and (8, G 4, D 256, page 1056). Values are seeded N(0,1)
-(synthetic data). L2 (129 MB) is flushed between timed steps by writing 512 MiB; the flush is
-outside the timed region.
+A step is one pass of the whole hot path over one batch: for every run (shape) of the
+workload, stage 1 (live key-tile bounds and work list) and the attention kernel, through the
+C ABI. The default workload is the mixed-serving sweep: one seeded batch of 32 sequences
+(context U[4096, 32768], query U[512, 4096], 32 q / 4 kv heads, D 128, causal) run at each page
+size 128, 512, 544, 1040, 1056 and 2048, without a window and with window_left 4096 (12 runs,
+bf16 KV; ``mixed_serving_fp8`` runs the same sweep over an fp8 e4m3 cache). Values are seeded
+N(0,1) (synthetic data). L2 (129 MB) is flushed between timed steps by writing 512 MiB; the
+flush is outside the timed region. The CPU-baseline leg times the oracle on sampled rows and
+compares those rows with the last timed step's output (``parity`` in the line).
 
 Prints one JSON line (rank 0). ``value`` is TFLOP/s over live (query, key) pairs:
 4 * D * Hq per pair, pairs counted by the library's own interval arithmetic.
@@ -43,6 +45,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ---------------------------------------------------------------------------------------
 def make_workload(name: str, seed: int):
     from paged_kv_prefix_gb300 import workloads as wl
+    if name in ("mixed_serving", "mixed_serving_fp8"):
+        kv = "fp8_e4m3" if name.endswith("fp8") else "bf16"
+        return ("mixed serving sweep: 32 seqs, ctx U[4096,32768], q U[512,4096], 32 q / 4 kv "
+                "heads, D 128, causal; one run per page size in {128,512,544,1040,1056,2048} x "
+                f"window_left in {{0,4096}} (12 runs, one seeded batch), {kv} KV cache"
+                + (" (one per-tensor fp32 scale each for K and V)" if kv != "bf16" else ""),
+                [wl.mixed(p, w, kv_dtype=kv, seed=seed) for w in (False, True)
+                 for p in wl.MIXED_PAGE_SIZES])
     if name == "nonpow2":
         return ("non-power-of-2 pages: 8 seqs, ctx U[0,8192], q U[1,2048], causal; "
                 "(Hq,G,D,P) = (64,1,128,544), (8,4,256,1040), (8,4,256,1056)",
@@ -298,10 +308,12 @@ def sum_over_ranks(dist, value: float, device) -> float:
 # ---------------------------------------------------------------------------------------
 def oracle_sample(cases, budget_s: float, rng_seed: int = 0):
     """Times the oracle on evenly spaced query tokens of each case until ~budget_s of CPU
-    work. Returns (live-pair FLOPs computed, seconds, description)."""
+    work. Returns (live-pair FLOPs computed, seconds, description, rows): ``rows`` lists, per
+    case, (sequence, query tokens, the oracle's output rows) of the last sample taken."""
     from oracle import ref
     flops, secs, tokens = 0.0, 0.0, 0
     per_case = budget_s / len(cases)
+    rows = []
     for case in cases:
         inp = case.numpy_inputs()
         cu = inp["cu_query_lens"]
@@ -312,11 +324,13 @@ def oracle_sample(cases, budget_s: float, rng_seed: int = 0):
         n = int(cu[b + 1] - cu[b])
         kv = (ref.gather_kv(inp, b, "k"), ref.gather_kv(inp, b, "v"))
         spent, count = 0.0, 2
+        last = None
         while spent < per_case and count <= n:
             toks = np.linspace(0, n - 1, num=min(count, n)).astype(np.int64)
             t0 = time.perf_counter()
-            ref.attention_rows(inp, b, toks, kv=kv)
+            out = ref.attention_rows(inp, b, toks, kv=kv)
             dt = time.perf_counter() - t0
+            last = (b, toks, out)
             pairs = int(ref.allowed_mask(c + toks, c + n, case.causal, case.window_left,
                                          case.window_right, None if inp["mm_ranges"] is None
                                          else inp["mm_ranges"][b], case.clamp_mm,
@@ -326,7 +340,26 @@ def oracle_sample(cases, budget_s: float, rng_seed: int = 0):
             tokens += len(toks)
             spent += dt
             count *= 2
-    return flops, secs, f"{tokens} query tokens (all heads) of the heaviest sequence of each shape"
+        rows.append(last)
+    return (flops, secs,
+            f"{tokens} query tokens (all heads) of the heaviest sequence of each shape", rows)
+
+
+def sampled_parity(cases, dcs, rows) -> dict:
+    """The oracle rows the CPU baseline computed, against the same rows of the timed run's
+    output: max abs error and the number of elements outside |err| <= 2e-2 + 2e-2 |want|."""
+    worst, bad, n_el = 0.0, 0, 0
+    for case, dc, r in zip(cases, dcs, rows):
+        if r is None:
+            continue
+        b, toks, want = r
+        q0 = int(case.cu_query_lens[b])
+        got = dc.out[q0 + toks].float().cpu().numpy()
+        err = np.abs(got - want)
+        worst = max(worst, float(err.max()))
+        bad += int((err > 2e-2 + 2e-2 * np.abs(want)).sum())
+        n_el += err.size
+    return {"parity_max_abs": worst, "elements_outside_2e-2": bad, "elements_checked": n_el}
 
 
 def cpu_cores() -> int:
@@ -349,7 +382,7 @@ def run_reference(args):
         oracle_sample(cases, per_step / 4)
     total_f, total_s, sample = 0.0, 0.0, ""
     for _ in range(args.steps):
-        f, s, sample = oracle_sample(cases, per_step)
+        f, s, sample, _ = oracle_sample(cases, per_step)
         total_f += f
         total_s += s
     tflops = total_f / total_s / 1e12
@@ -379,6 +412,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     binding.lib()
     desc, cases = make_workload(args.workload, seed=rank)
+    if args.runs:  # a subset of the workload's runs (e.g. one launch for a profiler)
+        keep = [int(x) for x in args.runs.split(",")]
+        cases = [cases[i] for i in keep]
+        desc += f"; runs {keep} only: " + ", ".join(c.name for c in cases)
     dcs = [binding.DeviceCase(c, device=dev, flags_extra=workload_flags(args.workload),
                               kv_split_tiles=16 if args.workload == "decode_split" else 0)
            for c in cases]
@@ -492,10 +529,13 @@ def run_ours(args):
                                     "gbs": round(gbs, 1), "peak": float(peaks["hbm_gbs"]),
                                     "frac": round(gbs / float(peaks["hbm_gbs"]), 4)}
     cpu = None
+    check = None
     if not args.no_cpu_baseline and world == 1:
-        f, s, sample = oracle_sample(cases, args.cpu_seconds)
+        f, s, sample, rows = oracle_sample(cases, args.cpu_seconds)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": sample + f" ({s:.1f} s)"}
+        # the rows the oracle just computed, against the output of the last timed step
+        check = sampled_parity(cases, dcs, rows)
     line = {
         "metric": METRIC,
         "value": value,
@@ -522,6 +562,7 @@ def run_ours(args):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+        line["parity"] = check
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -537,8 +578,15 @@ def run_e2e(args, cases, dcs, step_flops, stream, dev):
              "context_lens"]
     host = []
     h2d = d2h = 0
+    pinned = {}  # one pinned copy per host tensor (runs of a sweep share their value tensors)
+
+    def pin(t):
+        if id(t) not in pinned:
+            pinned[id(t)] = t.pin_memory()
+        return pinned[id(t)]
+
     for case, dc in zip(cases, dcs):
-        hs = {n: getattr(case, n).pin_memory() for n in names}
+        hs = {n: pin(getattr(case, n)) for n in names}
         if case.mm_ranges is not None:
             hs["mm_ranges"] = case.mm_ranges.pin_memory()
         hs["k_scale"] = torch.tensor([case.k_scale], dtype=torch.float32).pin_memory()
@@ -663,7 +711,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="nonpow2")
+    ap.add_argument("--workload", default="mixed_serving")
+    ap.add_argument("--runs", default="",
+                    help="comma-separated indices: run only these runs (shapes) of the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)

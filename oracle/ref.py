@@ -78,7 +78,6 @@ __all__ = [
     "attention_rows",
     "tile_bounds",
     "live_pairs",
-    "num_qtiles",
 ]
 
 
@@ -337,13 +336,8 @@ def append_kv(inp: dict) -> tuple:
 # ---------------------------------------------------------------------------------------
 # Live key tiles and live pairs, by brute force over the dense mask.
 # ---------------------------------------------------------------------------------------
-def num_qtiles(inp: dict, tq: int) -> int:
-    cu = inp["cu_query_lens"]
-    return int(sum(-(-int(cu[b + 1] - cu[b]) // tq) for b in range(len(cu) - 1)))
-
-
 def tile_bounds(inp: dict, tq: int, tn: int) -> np.ndarray:
-    """``[num_qtiles, 2]`` int32: for each (sequence, query tile of ``tq`` tokens) in order,
+    """``[query tiles, 2]`` int32: for each (sequence, query tile of ``tq`` tokens) in order,
     ``lo = min(K*) // tn`` and ``hi = max(K*) // tn + 1`` where ``K*`` is the set of keys
     that at least one query of the tile may attend to."""
     cu = inp["cu_query_lens"]

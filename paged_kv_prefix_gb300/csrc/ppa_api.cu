@@ -360,12 +360,14 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   }
   if (e == cudaSuccess && w.split) {  // segments of split sequences -> the output rows
     ppa::MergeParams m{};
+    m.ws = a.ws;
     m.part_o = a.part_o;
     m.part_lse = a.part_lse;
     m.seq_split_base = reinterpret_cast<const int32_t*>(ws + w.seq_split_base);
     m.cu_query_lens = cu_query_lens;
     m.out = out;
     m.num_seqs = dims->num_seqs;
+    m.total_q = dims->total_q;
     m.num_kv_heads = dims->num_kv_heads;
     m.group = G;
     m.head_dim = D;

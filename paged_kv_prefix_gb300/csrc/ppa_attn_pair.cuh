@@ -727,18 +727,26 @@ cudaError_t launch_attn_pair(const AttnParams& p, int max_items, cudaStream_t st
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // per-device set-up, once; under a lock so that a concurrent first call cannot read
+  // sm_count before it is written
+  static std::mutex mu;
   static int configured[64] = {0};
   static int sm_count[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_pair_kernel<D, FP8, SPLIT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(attn_pair_kernel<D, FP8, SPLIT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      configured[dev] = 1;
+    }
+    sms = sm_count[dev];
   }
-  const int pairs = max(1, min(sm_count[dev] / 2, max_items));
+  const int pairs = max(1, min(sms / 2, max_items));
   attn_pair_kernel<D, FP8, SPLIT><<<2 * pairs, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "ppa_internal.cuh"
 #include "ppa_kernels.h"
@@ -978,18 +979,26 @@ cudaError_t launch_attn_ws(const AttnParams& p, int max_items, cudaStream_t stre
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // per-device set-up, once; under a lock so that a concurrent first call cannot read
+  // sm_count before it is written
+  static std::mutex mu;
   static int configured[64] = {0};
   static int sm_count[64] = {0};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attn_ws_kernel<D, FP8, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(attn_ws_kernel<D, FP8, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      configured[dev] = 1;
+    }
+    sms = sm_count[dev];
   }
-  const int grid = max(1, min(sm_count[dev], max_items));
+  const int grid = max(1, min(sms, max_items));
   attn_ws_kernel<D, FP8, SPLIT><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

@@ -142,12 +142,13 @@ cudaError_t launch_append_kv(const AppendParams& p, cudaStream_t stream);
 // Split-KV merge (ppa_stage1.cu): for every split sequence and KV head, the segments' partial
 // rows combined by their log-sum-exps into the bf16 output.
 struct MergeParams {
+  const WsHeader* ws;  // the plan's header: n_items == 0 after the plan rejected the batch
   const float* part_o;
   const float* part_lse;
   const int32_t* seq_split_base;  // [B + 1]
   const int32_t* cu_query_lens;
   void* out;  // bf16 [total_q][Hq][D]
-  int num_seqs, num_kv_heads, group, head_dim, num_q_heads;
+  int num_seqs, total_q, num_kv_heads, group, head_dim, num_q_heads;
 };
 cudaError_t launch_split_merge(const MergeParams& p, cudaStream_t stream);
 

@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
   }
   __syncthreads();
   if (s_err || n_units > p.max_units || (long long)n_units * p.num_kv_heads > INT_MAX) {
+    if (p.seq_split_base != nullptr)  // no segment of a rejected batch is merged
+      for (int b = tid; b <= B; b += kStage1Threads) p.seq_split_base[b] = 0;
     if (tid == 0) {
       report(p.status, PPA_ERR_INVALID);
       p.ws->n_items = 0;
@@ -461,13 +463,19 @@ cudaError_t launch_row_bounds(const MaskParams& mp, int num_seqs, int total_q, c
 // Split-KV merge: one CTA per (sequence, KV head), threads over the head dimension. For each
 // of the tile's rows, the segments' rows O_s (already divided by their own row sums) weigh in
 // with 2^(lse_s - max lse): softmax over the union of the segments' keys, exactly.
+// A plan that rejected the batch (bad lengths found on the device) leaves no items and no
+// partials: the merge then writes nothing. Rows are also bounded by one query tile and by
+// total_q, so lengths that changed after the plan cannot send a store outside `out`.
 __global__ void split_merge_kernel(const MergeParams p) {
+  if (p.ws->n_items == 0) return;
   const int b = blockIdx.x / p.num_kv_heads;
   const int g = blockIdx.x - b * p.num_kv_heads;
   const int s0 = p.seq_split_base[b], ns = p.seq_split_base[b + 1] - s0;
   if (ns <= 0) return;
   const int q0 = p.cu_query_lens[b];
-  const int rows = (p.cu_query_lens[b + 1] - q0) * p.group;  // <= kRowsPerTile
+  const int n = p.cu_query_lens[b + 1] - q0;
+  if (q0 < 0 || n <= 0 || n > p.total_q - q0) return;
+  const int rows = min(n * p.group, kRowsPerTile);
   for (int r = 0; r < rows; ++r) {
     float mx = -__int_as_float(0x7f800000);
     for (int s = 0; s < ns; ++s)

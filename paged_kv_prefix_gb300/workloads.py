@@ -163,6 +163,45 @@ def _quantize_e4m3(x: torch.Tensor) -> tuple[torch.Tensor, float]:
     return y.to(torch.float8_e4m3fn).view(torch.uint8), float(scale)
 
 
+# The last value draw, reused by the next case with the same seed, lengths and head shape (the
+# mixed-serving runs differ only in page size and window, so their values are identical).
+_VALUE_MEMO: dict = {}
+
+
+def _draw_values(seed_key, ctx: np.ndarray, qlen: np.ndarray, Hq: int, Hkv: int, D: int,
+                 logit_jump: Optional[tuple]):
+    """Q, k_new, v_new and every sequence's context K/V, drawn N(0, 1) in a fixed order from
+    ``default_rng(seed_key)``; with ``logit_jump`` the Q and K values are then shaped as
+    described in :func:`build_case`."""
+    key = (seed_key if isinstance(seed_key, int) else tuple(seed_key), tuple(ctx.tolist()),
+           tuple(qlen.tolist()), Hq, Hkv, D, logit_jump)
+    if _VALUE_MEMO.get("key") == key:
+        return _VALUE_MEMO["values"]
+    _VALUE_MEMO.clear()
+    rng = np.random.default_rng(seed_key)
+    total_q = int(qlen.sum())
+    q = _normal_bf16(rng, (total_q, Hq, D))
+    k_new = _normal_bf16(rng, (total_q, Hkv, D))
+    v_new = _normal_bf16(rng, (total_q, Hkv, D))
+    ctx_k = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
+    ctx_v = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
+    if logit_jump is not None:
+        boost, first, period, q_noise = logit_jump
+        q = (q.float() * q_noise).to(torch.bfloat16)
+        q[:, :, 0] = 1.0
+        cu = np.concatenate([[0], np.cumsum(qlen)])
+        for b in range(ctx.size):
+            c, n = int(ctx[b]), int(qlen[b])
+            pos = np.arange(c + n)
+            col = np.where((pos >= first) & ((pos - first) % period == 0), boost, 0.0)
+            col = torch.from_numpy(col.astype(np.float32)).to(torch.bfloat16)
+            ctx_k[b][:, :, 0] = col[:c, None]
+            k_new[int(cu[b]):int(cu[b]) + n, :, 0] = col[c:, None]
+    values = (q, k_new, v_new, ctx_k, ctx_v)
+    _VALUE_MEMO.update(key=key, values=values)
+    return values
+
+
 def build_case(
     name: str,
     context_lens: Sequence[int],
@@ -185,8 +224,16 @@ def build_case(
     chunk_size: int = 0,
     chunk_lookback: int = 0,
     seq_causal: Optional[Sequence[bool]] = None,
+    logit_jump: Optional[tuple] = None,
 ) -> PrefillCase:
-    """Build one case. Lengths are per sequence; ``mm_ranges`` is ``[B, R, 2]`` or None."""
+    """Build one case. Lengths are per sequence; ``mm_ranges`` is ``[B, R, 2]`` or None.
+
+    ``logit_jump = (boost, first, period, q_noise)`` shapes Q and K so that a row's scores
+    jump upward once it reaches a sparse set of keys: every query row becomes
+    ``(1, q_noise * N(0,1), ...)`` (column 0 set to 1, the rest scaled down) and column 0 of
+    every key is 0, except at absolute positions ``first, first + period, ...`` of each
+    sequence, where it is ``boost``. Those keys' scores then exceed the others' by about
+    ``boost`` (times the softmax scale), while the rest stay close together."""
     ctx = np.asarray(context_lens, dtype=np.int64)
     qlen = np.asarray(query_lens, dtype=np.int64)
     assert ctx.shape == qlen.shape and ctx.ndim == 1
@@ -195,16 +242,14 @@ def build_case(
     P = int(page_size)
     D = int(head_dim)
     Hq, Hkv = int(num_q_heads), int(num_kv_heads)
-    rng = np.random.default_rng(seed if value_rng_seed is None else value_rng_seed)
     layout_rng = np.random.default_rng([seed, 7919])
 
     total_q = int(qlen.sum())
     cu = np.zeros(B + 1, dtype=np.int64)
     cu[1:] = np.cumsum(qlen)
 
-    q = _normal_bf16(rng, (total_q, Hq, D))
-    k_new = _normal_bf16(rng, (total_q, Hkv, D))
-    v_new = _normal_bf16(rng, (total_q, Hkv, D))
+    q, k_new, v_new, ctx_k, ctx_v = _draw_values(
+        seed if value_rng_seed is None else value_rng_seed, ctx, qlen, Hq, Hkv, D, logit_jump)
 
     # Pages owned by each sequence cover every position 0..s-1.
     s = ctx + qlen
@@ -221,10 +266,7 @@ def build_case(
         block_table[b, : pages_per_seq[b]] = perm[off : off + pages_per_seq[b]]
         off += pages_per_seq[b]
 
-    # Context K/V values, contiguous per sequence, then scattered into their pages.
-    ctx_k = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
-    ctx_v = [_normal_bf16(rng, (int(c), Hkv, D)) for c in ctx]
-
+    # Context K/V values (contiguous per sequence) are scattered into their pages.
     if kv_dtype == "bf16":
         fill = float("nan") if poison else 0.0
         k_cache = torch.full((num_pages, P, Hkv, D), fill, dtype=torch.bfloat16)
