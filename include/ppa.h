@@ -259,6 +259,24 @@ ppa_status ppa_live_kv_tokens(const ppa_dims* dims, const int32_t* cu_query_lens
  * conversion (exact; NaN codes give a bf16 NaN). */
 ppa_status ppa_debug_e4m3_to_bf16(const uint8_t* codes, uint16_t* bf16_out, int n, void* stream);
 
+/* Testing the bounded device-side waits without a fault. Every wait inside the attention
+ * kernels is bounded; when one runs out, the kernel stores PPA_ERR_TIMEOUT in *device_status,
+ * every warp leaves its loop, the copies still in flight are waited for (bounded again), the
+ * tensor-core operations retire, TMEM is freed and the kernel returns, so the context stays
+ * usable and the next call on the stream runs normally. This entry point runs ppa_prefill
+ * (same arguments) with every such wait limited to wait_limit_us microseconds (> 0), and
+ * with the query loader of the CTA that takes the plan's first work item never loading that
+ * item's query tiles nor fetching further work: the waits for them run out. The output is then unspecified. Head dims 64 and 128 (the
+ * single-CTA kernel) only; head_dim 256 returns PPA_ERR_UNSUPPORTED. The pages have no
+ * counterpart of this entry point: it exercises the library's own failure path. */
+ppa_status ppa_debug_prefill_stalled(const ppa_dims* dims, const void* q, const void* k_new,
+                                     const void* v_new, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* cu_query_lens,
+                                     const int32_t* context_lens, const int32_t* mm_ranges,
+                                     const float* k_scale, const float* v_scale, void* out,
+                                     void* workspace, int32_t* device_status,
+                                     unsigned wait_limit_us, void* stream);
+
 /* Synchronises `stream`, returns the code stored in *device_status and clears it to 0.
  * Returns PPA_ERR_CUDA if the synchronisation or the copy fails. */
 ppa_status ppa_read_status(int32_t* device_status, void* stream);

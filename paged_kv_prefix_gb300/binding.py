@@ -79,6 +79,8 @@ _SIGNATURES = {
     "ppa_live_pairs": (_I, [_DIMS, _P, _P, _P, _P, _P]),
     "ppa_live_kv_tokens": (_I, [_DIMS, _P, _P, _P, _P, _P]),
     "ppa_debug_e4m3_to_bf16": (_I, [_P, _P, _I, _P]),
+    "ppa_debug_prefill_stalled": (_I, [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, ctypes.c_uint, _P]),
     "ppa_read_status": (_I, [_P, _P]),
     "ppa_status_string": (ctypes.c_char_p, [_I]),
     "ppa_version": (_I, []),
@@ -249,6 +251,24 @@ def ppa_debug_e4m3_to_bf16(codes, bf16_out, n: int, stream=None, check: bool = T
     code = lib().ppa_debug_e4m3_to_bf16(_ptr(codes), _ptr(bf16_out), n, _stream(stream))
     if check:
         _check(code, "ppa_debug_e4m3_to_bf16")
+    return code
+
+
+def ppa_debug_prefill_stalled(dims: PpaDims, q, k_new, v_new, k_cache, v_cache, block_table,
+                              cu_query_lens, context_lens, mm_ranges, k_scale, v_scale, out,
+                              workspace, device_status, wait_limit_us: int, stream=None,
+                              check: bool = True) -> int:
+    """ppa_prefill with its device waits limited to ``wait_limit_us`` and the first CTA's
+    query load withheld, so that the waits run out (tests of the timeout path)."""
+    code = lib().ppa_debug_prefill_stalled(ctypes.byref(dims), _ptr(q), _ptr(k_new),
+                                           _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_table), _ptr(cu_query_lens),
+                                           _ptr(context_lens), _ptr(mm_ranges), _ptr(k_scale),
+                                           _ptr(v_scale), _ptr(out), _ptr(workspace),
+                                           _ptr(device_status), int(wait_limit_us),
+                                           _stream(stream))
+    if check:
+        _check(code, "ppa_debug_prefill_stalled")
     return code
 
 

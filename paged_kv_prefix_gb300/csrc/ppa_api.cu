@@ -237,11 +237,18 @@ ppa_status ppa_plan(const ppa_dims* dims, const int32_t* cu_query_lens,
   return PPA_OK;
 }
 
-ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
-                      const void* k_cache, const void* v_cache, const int32_t* block_table,
-                      const int32_t* cu_query_lens, const int32_t* context_lens,
-                      const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
-                      void* out, void* workspace, int32_t* device_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// ppa_attend with the attention kernel's wait limit and the test stall of
+// ppa_debug_prefill_stalled.
+ppa_status attend_impl(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* cu_query_lens, const int32_t* context_lens,
+                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                       void* out, void* workspace, int32_t* device_status, void* stream,
+                       unsigned long long wait_ns, int stall) {
   const ppa_status st = check_dims(dims);
   if (st != PPA_OK) return st;
   const bool in_cache = kv_in_cache(dims);
@@ -295,6 +302,8 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   a.page_size = dims->page_size;
   a.num_pages = dims->num_pages;
   a.max_pages_per_seq = dims->max_pages_per_seq;
+  a.wait_ns = wait_ns;
+  a.debug_stall = stall;
   const int D = dims->head_dim;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // fp8 with scratch: dequantise the live cache tiles once, then run the bf16 kernel on them,
@@ -377,12 +386,11 @@ ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, co
   return e == cudaSuccess ? PPA_OK : PPA_ERR_CUDA;
 }
 
-ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
-                       const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       const int32_t* cu_query_lens, const int32_t* context_lens,
-                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
-                       void* out, void* workspace, int32_t* device_status, void* stream) {
-  // Validate everything ppa_attend checks before ppa_plan launches anything.
+// Host checks of ppa_prefill, before ppa_plan launches anything.
+ppa_status prefill_checks(const ppa_dims* dims, const void* q, const void* k_new,
+                          const void* v_new, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const float* k_scale, const float* v_scale,
+                          const void* out) {
   const ppa_status st = check_dims(dims);
   if (st != PPA_OK) return st;
   const bool in_cache = kv_in_cache(dims);
@@ -395,6 +403,52 @@ ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, c
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return PPA_ERR_INVALID;
   if (!in_cache && (!aligned16(k_new) || !aligned16(v_new))) return PPA_ERR_INVALID;
+  return PPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ppa_status ppa_attend(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                      const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      const int32_t* cu_query_lens, const int32_t* context_lens,
+                      const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                      void* out, void* workspace, int32_t* device_status, void* stream) {
+  return attend_impl(dims, q, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
+                     context_lens, mm_ranges, k_scale, v_scale, out, workspace, device_status,
+                     stream, ppa::kWaitNs, 0);
+}
+
+ppa_status ppa_debug_prefill_stalled(const ppa_dims* dims, const void* q, const void* k_new,
+                                     const void* v_new, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* cu_query_lens,
+                                     const int32_t* context_lens, const int32_t* mm_ranges,
+                                     const float* k_scale, const float* v_scale, void* out,
+                                     void* workspace, int32_t* device_status,
+                                     unsigned wait_limit_us, void* stream) {
+  if (dims != nullptr && dims->head_dim == 256) return PPA_ERR_UNSUPPORTED;
+  if (wait_limit_us == 0) return PPA_ERR_INVALID;
+  const ppa_status sc = prefill_checks(dims, q, k_new, v_new, k_cache, v_cache, block_table,
+                                       k_scale, v_scale, out);
+  if (sc != PPA_OK) return sc;
+  const ppa_status sp = ppa_plan(dims, cu_query_lens, context_lens, mm_ranges, workspace,
+                                 device_status, stream);
+  if (sp != PPA_OK) return sp;
+  return attend_impl(dims, q, k_new, v_new, k_cache, v_cache, block_table, cu_query_lens,
+                     context_lens, mm_ranges, k_scale, v_scale, out, workspace, device_status,
+                     stream, 1000ull * wait_limit_us, 1);
+}
+
+ppa_status ppa_prefill(const ppa_dims* dims, const void* q, const void* k_new, const void* v_new,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* cu_query_lens, const int32_t* context_lens,
+                       const int32_t* mm_ranges, const float* k_scale, const float* v_scale,
+                       void* out, void* workspace, int32_t* device_status, void* stream) {
+  // Validate everything ppa_attend checks before ppa_plan launches anything.
+  const ppa_status sc = prefill_checks(dims, q, k_new, v_new, k_cache, v_cache, block_table,
+                                       k_scale, v_scale, out);
+  if (sc != PPA_OK) return sc;
   const ppa_status sp = ppa_plan(dims, cu_query_lens, context_lens, mm_ranges, workspace,
                                  device_status, stream);
   if (sp != PPA_OK) return sp;

@@ -79,7 +79,7 @@ struct PairShared {
     while (true) {
       if (mbar_try_wait_cluster(b, parity)) return true;
       if (*ws.abort) return false;
-      if (globaltimer_ns() - t0 > PPA_WAIT_NS) {
+      if (globaltimer_ns() - t0 > ws.limit) {
         *ws.abort = 1;
         report(ws.status, PPA_ERR_TIMEOUT);
         return false;
@@ -294,6 +294,14 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
     if (!ok) break;
   }
   cp_async_wait<0>();
+  // This warp's TMA copies land before the CTA exits: wait (bounded) for the last fill of
+  // every stage (see ws_producer).
+  if (lane == 0) {
+    for (uint32_t s = 0; s < static_cast<uint32_t>(ns) && s < kv_iter; ++s) {
+      const uint32_t f = s + ns * ((kv_iter - 1 - s) / ns);
+      sh.ws.drain(full_bar + 8 * s, (f / ns) & 1);
+    }
+  }
 }
 
 // Q loader (warp 10 of each CTA): this CTA's query tile of each unit; in the even CTA, lane 0
@@ -306,6 +314,7 @@ __device__ void pair_qloader(const AttnParams& p, const PairShared& sh, uint32_t
   const int lane = threadIdx.x & 31;
   if (lane == 0) tma_prefetch_desc(&p.tm.q);
   uint32_t q_phase = 0;
+  bool loaded = false;
   for (int k = 0;; ++k) {
     if (sh.rank == 0 && lane == 0) pair_ring_put(sh, p, k, n_items);
     const int item = pair_ring_get(sh, k);
@@ -313,6 +322,7 @@ __device__ void pair_qloader(const AttnParams& p, const PairShared& sh, uint32_t
     const UnitInfo u = decode_item(p, item);
     if (!wait_warp(sh.ws, wsbar::Q_EMPTY, q_phase ^ 1)) break;
     q_phase ^= 1;
+    loaded = true;
     if (lane == 0) {  // rows past the sequence read zeros or foreign rows; the mask drops them
       const uint32_t box_bytes = static_cast<uint32_t>(p.group * p.tq * 128);
       mbar_arrive_expect_tx(sh.bar(wsbar::Q_FULL), (D / 64) * box_bytes);
@@ -322,6 +332,7 @@ __device__ void pair_qloader(const AttnParams& p, const PairShared& sh, uint32_t
                     u.q_start + (u.t0 + static_cast<int>(sh.rank)) * p.tq, sh.bar(wsbar::Q_FULL));
     }
   }
+  if (loaded && lane == 0) sh.ws.drain(wsbar::Q_FULL, q_phase ^ 1);  // the last load landed
 }
 
 // ---------------------------------------------------------------------------------------
@@ -634,6 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   sh.ws.abort = reinterpret_cast<volatile int*>(barp + wsbar::ABORT);
   sh.ws.ring = reinterpret_cast<volatile int*>(barp + wsbar::RING);
   sh.ws.status = p.status;
+  sh.ws.limit = p.wait_ns;
   sh.rank = cluster_ctarank();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -694,15 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
     pair_qloader<D>(p, sh, base, n_items);
   }
   // TMEM of both CTAs is written by the even CTA's MMAs: both wait for them to retire.
-  if (tid == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(sh.bar(wsbar::FIN), 0)) {
-      if (globaltimer_ns() - t0 > PPA_WAIT_NS) {
-        report(p.status, PPA_ERR_TIMEOUT);
-        break;
-      }
-    }
-  }
+  if (tid == 0 && !sh.ws.drain(wsbar::FIN, 0)) report(p.status, PPA_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no arrival or store from the peer is still in flight

@@ -10,6 +10,7 @@
 namespace ppa {
 
 constexpr int kRowsPerTile = 128;  // rows of one query tile (tokens x heads of a group)
+constexpr unsigned long long kWaitNs = 2000000000ull;  // default limit of a device wait: 2 s
 
 // Mask parameters of one call.
 struct MaskParams {

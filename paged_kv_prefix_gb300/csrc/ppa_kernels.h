@@ -75,6 +75,8 @@ struct AttnParams {
   MaskParams mask;
   int num_q_heads, num_kv_heads, group, tq, page_size, num_pages, max_pages_per_seq;
   float scale_log2;  // softmax scale * log2(e)
+  unsigned long long wait_ns;  // limit of every bounded wait in the attention kernels
+  int debug_stall;  // testing (single-CTA kernel): the CTA taking item 0 never loads its queries
 };
 
 cudaError_t launch_plan(const Stage1Params& p, cudaStream_t stream);

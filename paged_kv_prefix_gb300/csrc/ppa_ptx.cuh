@@ -2,16 +2,13 @@
 // attention kernel uses: mbarriers, cp.async, fences between the generic and async
 // proxies, Tensor Memory (TMEM) allocation and tcgen05 MMA / load / store.
 //
-// Every wait here is bounded: it gives up after PPA_WAIT_NS of wall time (read from
-// %globaltimer) and reports failure to the caller, which records PPA_ERR_TIMEOUT and skips
-// the rest of its work instead of spinning forever.
+// The kernels bound every wait built on these: it gives up after a limit of wall time (read
+// from %globaltimer; kWaitNs unless the launch sets another) and reports failure to the
+// caller, which records PPA_ERR_TIMEOUT and skips the rest of its work instead of spinning
+// forever.
 #pragma once
 
 #include <cstdint>
-
-#ifndef PPA_WAIT_NS
-#define PPA_WAIT_NS 2000000000ull  // 2 s
-#endif
 
 namespace ppa {
 
@@ -59,16 +56,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// Waits for the phase with the given parity to complete. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > PPA_WAIT_NS) return false;
-  }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
