@@ -57,6 +57,7 @@ struct PairCfg {
   static_assert(keys_per_tile(D) == TN, "plan and kernel agree on the key tile");
 };
 
+
 namespace pairbar {
 constexpr int KQ_READY = 272;   // both CTAs' Q of the unit resident
 constexpr int KREADY = 280;     // [NSK] both CTAs' halves of the K stage resident
@@ -64,6 +65,7 @@ constexpr int KREADY = 280;     // [NSK] both CTAs' halves of the K stage reside
 // odd CTA the same without the MMA warp
 constexpr int kConsumers = 21;
 }  // namespace pairbar
+static_assert(pairbar::KREADY + 8 * PairCfg<256>::NSK <= wsbar::LIMIT, "barrier block layout");
 
 struct PairShared {
   WsShared ws;
@@ -79,7 +81,7 @@ struct PairShared {
     while (true) {
       if (mbar_try_wait_cluster(b, parity)) return true;
       if (*ws.abort) return false;
-      if (globaltimer_ns() - t0 > ws.limit) {
+      if (globaltimer_ns() - t0 > ws.limit()) {
         *ws.abort = 1;
         report(ws.status, PPA_ERR_TIMEOUT);
         return false;
@@ -645,7 +647,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
   sh.ws.abort = reinterpret_cast<volatile int*>(barp + wsbar::ABORT);
   sh.ws.ring = reinterpret_cast<volatile int*>(barp + wsbar::RING);
   sh.ws.status = p.status;
-  sh.ws.limit = p.wait_ns;
   sh.rank = cluster_ctarank();
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -670,6 +671,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
     mbar_init(sh.bar(O_DONE), 1);
     mbar_init(sh.bar(O_EMPTY), 8);
     mbar_init(sh.bar(FIN), 1);
+    *reinterpret_cast<unsigned long long*>(barp + LIMIT) = p.wait_ns;
     mbar_init(sh.bar(pairbar::KQ_READY), 2);
     for (int s = 0; s < C::NSK; ++s) mbar_init(sh.bar(pairbar::KREADY + 8 * s), 2);
     *sh.ws.abort = 0;

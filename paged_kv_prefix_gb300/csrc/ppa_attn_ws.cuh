@@ -85,7 +85,7 @@ constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL 
               V_FULL = 80, K_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
               O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224,
               V_EMPTY = 240, FOLD = 288,  // FOLD: fp8 scale constants, see Fp8Fold
-              UNITS = 320;  // single-CTA kernel: the two ring slots' decoded units (2 x 64 B)
+              LIMIT = 304;  // u64: ns before a wait gives up (read only once a wait is slow)
 constexpr int kRingConsumers = 14;  // warps 0..13 each release a ring slot once
 }  // namespace wsbar
 
@@ -94,8 +94,13 @@ struct WsShared {
   volatile int* abort;
   volatile int* ring;
   int32_t* status;
-  unsigned long long limit;  // ns before a wait gives up
   __device__ uint32_t bar(int off) const { return bars + off; }
+  // The wait limit, kept in shared memory rather than in every role's registers.
+  __device__ unsigned long long limit() const {
+    unsigned long long v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(bars + wsbar::LIMIT));
+    return v;
+  }
   // Bounded wait; false if the CTA is aborting (this or another role timed out).
   __device__ bool wait(int off, uint32_t parity) const {
     const uint32_t b = bars + off;
@@ -104,7 +109,7 @@ struct WsShared {
     while (true) {
       if (mbar_try_wait(b, parity)) return true;
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit) {
+      if (globaltimer_ns() - t0 > limit()) {
         *abort = 1;
         report(status, PPA_ERR_TIMEOUT);
         return false;
@@ -117,7 +122,7 @@ struct WsShared {
     const uint32_t b = bars + off;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(b, parity))
-      if (globaltimer_ns() - t0 > limit) return false;
+      if (globaltimer_ns() - t0 > limit()) return false;
     return true;
   }
 };
@@ -129,13 +134,46 @@ __device__ __forceinline__ bool wait_warp(const WsShared& sh, int off, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Consumer side of the item ring (whole warp): the k-th item of this CTA, or -1 at the end.
+__device__ __forceinline__ int ring_get(const WsShared& sh, int k) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
+  item = __shfl_sync(0xffffffffu, item, 0);  // one outcome for the whole warp
+  if ((threadIdx.x & 31) == 0) mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
+  return item;
+}
+
+// Single-thread consumer (the MMA issuer): same protocol without the warp.
+__device__ __forceinline__ int ring_get1(const WsShared& sh, int k) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
+  mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
+  return item;
+}
+
+// Producer side (one thread): fetch the next item and publish it in slot k & 1. Returns the
+// item (-1: none left).
+__device__ __forceinline__ int ring_put(const WsShared& sh, const AttnParams& p, int k,
+                                        int n_items) {
+  const int slot = k & 1;
+  int item = -1;
+  if (sh.wait(wsbar::ITEM_EMPTY + 8 * slot, ((k >> 1) & 1) ^ 1)) {
+    item = atomicAdd(&p.ws->next_item, 1);
+    if (item >= n_items) item = -1;
+  }
+  sh.ring[slot] = item;
+  mbar_arrive(sh.bar(wsbar::ITEM_FULL + 8 * slot));
+  return item;
+}
+
 struct UnitInfo {
   int b, g, t0, nt, c, n, s, q_start, lo, hi;
   int cs;  // key positions below cs come from the cache: c, or s when K/V are in the cache
   int part;  // split-KV segment: partial-result slot, -1 when the unit writes the output
   int lo_i[2], hi_i[2];
 };
-static_assert(sizeof(UnitInfo) == 64, "one ring slot of the single-CTA kernel");
 
 __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   UnitInfo u;
@@ -158,69 +196,6 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   u.lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
   u.hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
   return u;
-}
-
-// The item ring of the single-CTA kernel. The Q loader's lane 0 takes the CTA's next item
-// from the plan (atomic work stealing) and decodes it once into the slot's UnitInfo; every
-// consumer copies the decoded unit out of shared memory, so a unit boundary costs the
-// consumers no dependent global loads (item -> unit -> sequence lengths).
-__device__ __forceinline__ volatile int* slot_words(const WsShared& sh, int slot) {
-  return reinterpret_cast<volatile int*>(reinterpret_cast<volatile char*>(sh.ring) +
-                                         (wsbar::UNITS - wsbar::RING) + 64 * slot);
-}
-
-// Field by field, so that the unit stays in registers (a copy through its address would
-// place it in local memory).
-__device__ __forceinline__ void read_slot(const WsShared& sh, int slot, UnitInfo& u) {
-  const volatile int* w = slot_words(sh, slot);
-  u.b = w[0]; u.g = w[1]; u.t0 = w[2]; u.nt = w[3]; u.c = w[4]; u.n = w[5]; u.s = w[6];
-  u.q_start = w[7]; u.lo = w[8]; u.hi = w[9]; u.cs = w[10]; u.part = w[11];
-  u.lo_i[0] = w[12]; u.lo_i[1] = w[13]; u.hi_i[0] = w[14]; u.hi_i[1] = w[15];
-}
-
-__device__ __forceinline__ void write_slot(const WsShared& sh, int slot, const UnitInfo& u) {
-  volatile int* w = slot_words(sh, slot);
-  w[0] = u.b; w[1] = u.g; w[2] = u.t0; w[3] = u.nt; w[4] = u.c; w[5] = u.n; w[6] = u.s;
-  w[7] = u.q_start; w[8] = u.lo; w[9] = u.hi; w[10] = u.cs; w[11] = u.part;
-  w[12] = u.lo_i[0]; w[13] = u.lo_i[1]; w[14] = u.hi_i[0]; w[15] = u.hi_i[1];
-}
-
-// Consumer side (whole warp): false at the end of the CTA's work (or on an abort).
-__device__ __forceinline__ bool ring_get(const WsShared& sh, int k, UnitInfo& u) {
-  const int slot = k & 1;
-  int item = -1;
-  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
-  item = __shfl_sync(0xffffffffu, item, 0);  // one outcome for the whole warp
-  if (item >= 0) read_slot(sh, slot, u);
-  __syncwarp();  // every lane's reads before the release
-  if ((threadIdx.x & 31) == 0) mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
-  return item >= 0;
-}
-
-// Single-thread consumer (the MMA issuer): same protocol without the warp.
-__device__ __forceinline__ bool ring_get1(const WsShared& sh, int k, UnitInfo& u) {
-  const int slot = k & 1;
-  int item = -1;
-  if (sh.wait(wsbar::ITEM_FULL + 8 * slot, (k >> 1) & 1)) item = sh.ring[slot];
-  if (item >= 0) read_slot(sh, slot, u);
-  mbar_arrive(sh.bar(wsbar::ITEM_EMPTY + 8 * slot));
-  return item >= 0;
-}
-
-// Producer side (one thread): fetch the next item, decode it into slot k & 1 and publish it.
-// Returns the item (-1: none left).
-__device__ __forceinline__ int ring_put(const WsShared& sh, const AttnParams& p, int k,
-                                        int n_items) {
-  const int slot = k & 1;
-  int item = -1;
-  if (sh.wait(wsbar::ITEM_EMPTY + 8 * slot, ((k >> 1) & 1) ^ 1)) {
-    item = atomicAdd(&p.ws->next_item, 1);
-    if (item >= n_items) item = -1;
-  }
-  if (item >= 0) write_slot(sh, slot, decode_item(p, item));
-  sh.ring[slot] = item;
-  mbar_arrive(sh.bar(wsbar::ITEM_FULL + 8 * slot));
-  return item;
 }
 
 // The allowed key interval of row j (query position c + j) of unit u: with multimodal ranges
@@ -428,8 +403,9 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const bool kv_fold = FP8 && fp8_fold(p).fold;
   uint32_t kv_iter = 0;
   for (int k = 0;; ++k) {
-    UnitInfo u;
-    if (!ring_get(sh, k, u)) break;
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
 
     // ---- this warp's rows of the K (or V) tiles of the union interval ----
     bool ok = true;
@@ -582,14 +558,13 @@ __device__ void ws_qloader(const AttnParams& p, const WsShared& sh, uint32_t bas
   uint32_t q_phase = 0;
   bool loaded = false;
   for (int k = 0;; ++k) {
-    int item = -1;
-    if (lane == 0) item = ring_put(sh, p, k, n_items);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    UnitInfo u;
-    if (!ring_get(sh, k, u)) break;
+    if (lane == 0) ring_put(sh, p, k, n_items);
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
     // Testing the bounded waits: the CTA that took the plan's first item neither loads its
     // queries nor feeds its ring any further, so the waits for them run out.
     if (p.debug_stall && item == 0) break;
+    const UnitInfo u = decode_item(p, item);
     if (!wait_warp(sh, wsbar::Q_EMPTY, q_phase ^ 1)) break;
     q_phase ^= 1;
     loaded = true;
@@ -632,8 +607,9 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   uint32_t kv_iter = 0, q_phase = 0, pf_bits = 0, oe_bits = 0;
   bool ok = true;
   for (int k = 0; ok; ++k) {
-    UnitInfo u;
-    if (!ring_get1(sh, k, u)) break;
+    const int item = ring_get1(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
     const int lo0 = u.lo_i[0], hi0 = u.hi_i[0], lo1 = u.lo_i[1], hi1 = u.hi_i[1];
     if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
     q_phase ^= 1;
@@ -773,8 +749,9 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
   uint32_t sf_phase = 0, od_phase = 0;
   uint32_t kv_next = 0;  // K/V ring position of the next unit's first key tile
   for (int k = 0;; ++k) {
-    UnitInfo u;
-    if (!ring_get(sh, k, u)) break;
+    const int item = ring_get(sh, k);
+    if (item < 0) break;
+    const UnitInfo u = decode_item(p, item);
     const uint32_t kv0 = kv_next;
     kv_next += u.hi - u.lo;
     if (i >= u.nt) continue;
@@ -943,7 +920,6 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
   sh.abort = reinterpret_cast<volatile int*>(barp + wsbar::ABORT);
   sh.ring = reinterpret_cast<volatile int*>(barp + wsbar::RING);
   sh.status = p.status;
-  sh.limit = p.wait_ns;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   if (tid == 0) {
@@ -968,6 +944,7 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     }
     mbar_init(sh.bar(FIN), 1);
     *sh.abort = 0;
+    *reinterpret_cast<unsigned long long*>(barp + LIMIT) = p.wait_ns;
     if constexpr (FP8) {
       const Fp8Fold f = fp8_fold(p);
       float* fc = reinterpret_cast<float*>(barp + FOLD);
