@@ -2,8 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mixed_serving|mixed_serving_fp8|nonpow2|swa64|swa1024|mm|mixed|
-                                mixed_fp8|mixed_window|mixed_cached|chunked|decode|decode_split]
-                    [--no-cpu-baseline] [--sweep windows|pages]
+                                mixed_fp8|mixed_window|mixed_cached|chunked|decode|decode_split|
+                                decode_fp8|decode_fp8_inkernel]
+                    [--no-cpu-baseline] [--sweep windows|pages|splits|groups]
 
 A step is one pass of the whole hot path over one batch: for every run (shape) of the
 workload, stage 1 (live key-tile bounds and work list) and the attention kernel, through the
@@ -73,6 +74,12 @@ def make_workload(name: str, seed: int):
         return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
                 "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
                 [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
+    if name in ("decode_fp8", "decode_fp8_inkernel"):
+        return ("decode over an fp8 e4m3 cache: 32 seqs, ctx U[8192,32768], 1 new token each, "
+                "32 q / 8 kv heads, D 128, page 544, causal; "
+                + ("e4m3 rows widened in the attention kernel" if name.endswith("inkernel")
+                   else "live cache tiles dequantised into workspace first"),
+                [wl.decode(seed=seed, kv_dtype="fp8_e4m3")])
     if name in ("decode", "decode_split"):
         return (f"decode: 32 seqs, ctx U[8192,32768], 1 new token each, 32 q / 8 kv heads, D 128, "
                 f"page 544, causal"
@@ -111,15 +118,27 @@ def _kv_in_cache(dc) -> bool:
 
 def _launches_per_step(dc) -> int:
     """Kernels of this library per step: the plan and the attention kernel, plus the fp8
-    live-tile marking and dequantisation kernels, plus the KV append, plus the split-KV
-    merge."""
-    return (2 + (2 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
+    live-tile marking, staging-slot and dequantisation kernels, plus the KV append, plus the
+    split-KV merge."""
+    return (2 + (3 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
             + (1 if dc.dims.kv_split_tiles > 0 else 0))
 
 
 def workload_flags(name: str) -> int:
     from paged_kv_prefix_gb300 import binding
-    return binding.PPA_FLAG_KV_IN_CACHE if name == "mixed_cached" else 0
+    if name == "mixed_cached":
+        return binding.PPA_FLAG_KV_IN_CACHE
+    return binding.PPA_FLAG_FP8_INKERNEL if name == "decode_fp8_inkernel" else 0
+
+
+def cache_token_bound(case, flags: int) -> int:
+    """ppa_dims.max_cache_tokens as a serving engine would pass it for an fp8 cache: the cached
+    positions of the batch (context, plus the new tokens when they are appended first)."""
+    from paged_kv_prefix_gb300 import binding
+    if case.kv_dtype == "bf16":
+        return 0
+    return int(case.context_lens.sum()) + (case.total_q if flags & binding.PPA_FLAG_KV_IN_CACHE
+                                           else 0)
 
 
 def append_bytes(case) -> float:
@@ -416,8 +435,10 @@ def run_ours(args):
         keep = [int(x) for x in args.runs.split(",")]
         cases = [cases[i] for i in keep]
         desc += f"; runs {keep} only: " + ", ".join(c.name for c in cases)
-    dcs = [binding.DeviceCase(c, device=dev, flags_extra=workload_flags(args.workload),
-                              kv_split_tiles=16 if args.workload == "decode_split" else 0)
+    flags = workload_flags(args.workload)
+    dcs = [binding.DeviceCase(c, device=dev, flags_extra=flags,
+                              kv_split_tiles=16 if args.workload == "decode_split" else 0,
+                              max_cache_tokens=cache_token_bound(c, flags))
            for c in cases]
     stream = torch.cuda.current_stream(dev)
 
@@ -705,6 +726,86 @@ def run_page_sweep(args):
             del dc
 
 
+def run_group_sweep(args):
+    """One ragged causal batch (8 sequences, context U[0, 8192], 1-2048 new tokens, page 544)
+    for every head dimension and GQA group size (8 KV heads, 8 * G query heads): how the tile
+    shape (a query tile holds 128 / G tokens of G heads) and the head dimension move the
+    tensor throughput. One JSON line per point."""
+    import torch
+    from paged_kv_prefix_gb300 import binding
+    from paged_kv_prefix_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(0)
+    ctx = rng.integers(0, 8193, size=8)
+    qlen = rng.integers(1, 2049, size=8)
+    for d in (64, 128, 256):
+        for g in (1, 2, 4, 8):
+            case = wl.build_case(f"groups_d{d}_g{g}", ctx, qlen, 8 * g, 8, d, 544, causal=True,
+                                 seed=0)
+            dc = binding.DeviceCase(case)
+            flops = algorithmic_flops(binding, dc, case, stream)
+            dc.plan(stream)
+            ms = []
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dc.attend(stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if k >= args.warmup:
+                    ms.append(e0.elapsed_time(e1))
+            st = dc.read_status(stream)
+            t = float(np.median(ms)) * 1e-3
+            print(json.dumps({"sweep": "head_dim_and_group", "head_dim": d, "group": g,
+                              "num_q_heads": 8 * g, "attend_ms": t * 1e3,
+                              "tflops": flops / t / 1e12,
+                              "frac_bf16": flops / t / 1e12 / float(peaks["bf16_tflops"]),
+                              "status": st}), flush=True)
+            del dc
+
+
+def run_split_sweep(args):
+    """Decode and verification batches (1 or 4 new tokens per sequence over 8K-32K contexts)
+    at several split-KV segment lengths (kv_split_tiles, 0 = unsplit): the time per launch
+    (plan, attention and merge) and the achieved HBM bandwidth. One JSON line per point."""
+    import torch
+    from paged_kv_prefix_gb300 import binding
+    from paged_kv_prefix_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for num_seqs in (8, 32):
+        for new_tokens in (1, 4):
+            case = wl.decode(seed=0, num_seqs=num_seqs, new_tokens=new_tokens)
+            for split in (0, 4, 8, 16, 32, 64, -1):
+                dc = binding.DeviceCase(case, kv_split_tiles=split)
+                nbytes = algorithmic_bytes(binding, dc, case, stream)
+                ms = []
+                for k in range(args.warmup + args.steps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    dc.run(stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if k >= args.warmup:
+                        ms.append(e0.elapsed_time(e1))
+                st = dc.read_status(stream)
+                t = float(np.median(ms)) * 1e-3
+                print(json.dumps({"sweep": "kv_split_tiles", "num_seqs": num_seqs,
+                                  "new_tokens": new_tokens, "kv_split_tiles": split,
+                                  "ms": t * 1e3, "gbs": nbytes / t / 1e9,
+                                  "frac_hbm": nbytes / t / 1e9 / float(peaks["hbm_gbs"]),
+                                  "workspace_mb": dc.workspace.numel() / 1e6, "status": st}),
+                      flush=True)
+                del dc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -717,7 +818,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
-    ap.add_argument("--sweep", choices=["windows", "pages"], default=None,
+    ap.add_argument("--sweep", choices=["windows", "pages", "splits", "groups"], default=None,
                     help="print one line per point of a window / length sweep instead")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -726,6 +827,10 @@ def main():
         run_window_sweep(args)
     elif args.sweep == "pages":
         run_page_sweep(args)
+    elif args.sweep == "splits":
+        run_split_sweep(args)
+    elif args.sweep == "groups":
+        run_group_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -114,21 +114,33 @@ typedef struct {
                           * than this many 128-key tiles is cut into segments of this many
                           * tiles, attended in parallel and merged by their log-sum-exps
                           * (the segmented mode the PR #53147 page names, tiles_per_segment).
-                          * 0: off. The workspace then holds the partial results. */
+                          * 0: off. -1: the library's tuned segment length (32 tiles). The
+                          * workspace then holds the partial results. */
   const int32_t* seq_causal; /* NULL, or a device array of num_seqs int32: sequence b's base
                               * mask is causal iff seq_causal[b] != 0, overriding
                               * PPA_FLAG_CAUSAL (per-sequence causality, USE_PER_SEQ_CAUSAL on
                               * the multimodal-pruning page). Read on the device by ppa_plan,
                               * ppa_attend and the mask/count entry points. */
+  int max_cache_tokens;  /* fp8 caches dequantised into workspace (no PPA_FLAG_FP8_INKERNEL):
+                          * > 0 sizes the bf16 staging by this bound instead of by every
+                          * block-table slot: at least the number of cached positions the
+                          * batch's queries may attend to, summed over sequences (the sum of
+                          * context_lens always suffices; windows make it smaller). Only the
+                          * key tiles those positions fall in are staged. If they need more
+                          * room on the device, the call stores PPA_ERR_INVALID and computes
+                          * nothing. 0: room for every block-table slot. */
 } ppa_dims;
 
 /* Bytes of device workspace ppa_prefill needs for `dims` (query-tile table and work list; with
  * multimodal ranges (max_mm_ranges > 0) also 8 bytes per query token: each row's allowed key
  * interval, written by ppa_plan so that the attention kernel does not rescan the ranges).
  * For an fp8 cache without PPA_FLAG_FP8_INKERNEL it also holds the bf16 scratch that the live
- * cache key tiles are dequantised into before the attention kernel runs: room for
- * num_seqs * ceil(max_pages_per_seq * page_size / 128) tiles of 128 positions for K and for
- * V (2 * 128 * num_kv_heads * head_dim * 2 bytes per tile), plus a block table and a bitmap.
+ * cache key tiles are dequantised into before the attention kernel runs: tiles of 128
+ * positions for K and for V (2 * 128 * num_kv_heads * head_dim * 2 bytes per tile), as many
+ * as floor(max_cache_tokens / 128) + 2 * num_seqs when max_cache_tokens > 0 (the live
+ * positions of a sequence are consecutive, so they touch at most that many tiles), else
+ * num_seqs * ceil(max_pages_per_seq * page_size / 128), never more than the latter; plus a
+ * table of num_seqs * ceil(max_pages_per_seq * page_size / 128) int32 and a bitmap.
  * If that bf16 staging does not fit the int32 row range, it is dropped and the fp8 path widens
  * in the kernel, as with the flag.
  * Returns 0 if dims is NULL or invalid. The caller allocates it; contents need no
@@ -286,8 +298,10 @@ const char* ppa_status_string(ppa_status status);
 
 /* Library version (major * 10000 + minor * 100 + patch). 0.2.0 added ppa_append_kv, the
  * PPA_FLAG_FP8_INKERNEL and PPA_FLAG_KV_IN_CACHE flags, and the ppa_dims fields chunk_size,
- * chunk_lookback and seq_causal (a layout change: callers built against 0.1 must rebuild). */
-#define PPA_VERSION 200
+ * chunk_lookback and seq_causal. 0.3.0 inserted kv_split_tiles before seq_causal and appended
+ * max_cache_tokens to ppa_dims (layout changes: callers built against 0.2 must rebuild), and
+ * added kv_split_tiles = -1, ppa_prefill_noalloc and ppa_debug_prefill_stalled. */
+#define PPA_VERSION 300
 int ppa_version(void);
 
 #ifdef __cplusplus

@@ -50,6 +50,7 @@ class PpaDims(ctypes.Structure):
         ("chunk_lookback", ctypes.c_int),
         ("kv_split_tiles", ctypes.c_int),
         ("seq_causal", ctypes.c_void_p),  # device int32[num_seqs] or None
+        ("max_cache_tokens", ctypes.c_int),
     ]
 
 
@@ -304,11 +305,13 @@ def dims_for(case, flags_extra: int = 0) -> PpaDims:
 class DeviceCase:
     """A case's tensors on the GPU plus the output, workspace and status buffers."""
 
-    def __init__(self, case, device="cuda", flags_extra: int = 0, kv_split_tiles: int = 0):
+    def __init__(self, case, device="cuda", flags_extra: int = 0, kv_split_tiles: int = 0,
+                 max_cache_tokens: int = 0):
         import torch
         self.case = case
         self.dims = dims_for(case, flags_extra)
-        self.dims.kv_split_tiles = kv_split_tiles  # sizes the workspace below
+        self.dims.kv_split_tiles = kv_split_tiles  # these two size the workspace below
+        self.dims.max_cache_tokens = max_cache_tokens
         dev = torch.device(device)
         self.q = case.q.to(dev)
         self.k_new = case.k_new.to(dev)

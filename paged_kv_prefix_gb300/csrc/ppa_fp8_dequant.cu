@@ -6,15 +6,15 @@
 // issue slots. Here each live tile is converted once, by a memory-bound kernel, and the
 // attention kernel then runs its bf16 path on the scratch.
 //
-// Scratch layout: "pages" of TN (=128) tokens, page b * tiles_per_seq + t holding cache
-// positions [t * TN, t * TN + TN) of sequence b, each position [Hkv][D] bf16 like the cache.
-// The identity block table (entry b * tiles_per_seq + t = b * tiles_per_seq + t) goes next
-// to it, so the attention kernel reads the scratch as a paged cache with page size TN whose
-// key tiles never straddle a page. Only tiles some unit visits are written; the attention
-// kernel reads no others (the same live-tile intervals drive both). Rows past a sequence's
-// cache positions (its context, or its context and new tokens when those were appended
-// first) are not written and not read: the attention kernel takes those keys from the
-// new-token tensors, or zero-fills positions past the sequence.
+// Scratch layout: "pages" of TN (=128) tokens, each holding the cache positions
+// [t * TN, t * TN + TN) of one live key tile t of one sequence b, each position [Hkv][D] bf16
+// like the cache. Only the live tiles (those some unit visits) get a page: they are packed in
+// sequence order, and a block table [num_seqs][tiles_per_seq] gives each live tile its page,
+// so the attention kernel reads the scratch as a paged cache with page size TN whose key tiles
+// never straddle a page (the same live-tile intervals drive both, so it reads no other entry).
+// Rows past a sequence's cache positions (its context, or its context and new tokens when
+// those were appended first) are not written and not read: the attention kernel takes those
+// keys from the new-token tensors, or zero-fills positions past the sequence.
 //
 // Each value is bf16(decode(code) * scale), the fp32 product rounded once, as in the
 // in-kernel path when it applies the scales itself.
@@ -57,16 +57,48 @@ __global__ void fp8_mark_kernel(Fp8DequantParams p) {
   }
 }
 
-// One CTA per (sequence, key tile) and tensor (blockIdx.y: 0 = K, 1 = V). Writes the identity
-// block-table entry, then, if the tile is live, the bf16 rows of its cache positions.
+// One CTA of 1024 threads: the staging page of every live tile, in sequence order (a scan of
+// the sequences' live-tile counts, then each sequence numbers its live tiles). If they need
+// more pages than the staging holds, the batch is rejected: PPA_ERR_INVALID, and the plan's
+// item count is cleared, so neither the dequantisation nor the attention does any work.
+constexpr int kSlotThreads = 1024;
+
+__global__ void __launch_bounds__(kSlotThreads) fp8_slots_kernel(Fp8DequantParams p) {
+  __shared__ int s_warp[32];
+  int carry = 0;
+  for (int b0 = 0; b0 < p.num_seqs; b0 += kSlotThreads) {
+    const int b = b0 + threadIdx.x;
+    const uint32_t* bits = p.live_bits + (size_t)b * p.words_per_seq;
+    int cnt = 0;
+    if (b < p.num_seqs)
+      for (int w = 0; w < p.words_per_seq; ++w) cnt += __popc(bits[w]);
+    int total;
+    const int excl = block_exclusive_scan(cnt, s_warp, &total);
+    if (b < p.num_seqs) {
+      int page = carry + excl;
+      int32_t* row = p.table + (size_t)b * p.tiles_per_seq;
+      for (int w = 0; w < p.words_per_seq; ++w) {
+        for (uint32_t m = bits[w]; m != 0u; m &= m - 1u) row[32 * w + __ffs(m) - 1] = page++;
+      }
+    }
+    carry += total;
+  }
+  if (carry > p.capacity && threadIdx.x == 0) {
+    report(p.status, PPA_ERR_INVALID);
+    p.ws->n_items = 0;
+  }
+}
+
+// One CTA per (sequence, key tile) and tensor (blockIdx.y: 0 = K, 1 = V): if the tile is live,
+// the bf16 rows of its cache positions into its staging page.
 constexpr int kDequantThreads = 256;
 
 __global__ void __launch_bounds__(kDequantThreads) fp8_dequant_kernel(Fp8DequantParams p) {
+  if (p.ws->n_items == 0) return;  // rejected by the slot pass (or an empty plan)
   const int b = blockIdx.x / p.tiles_per_seq;
   const int t = blockIdx.x - b * p.tiles_per_seq;
-  const int page = blockIdx.x;  // = b * tiles_per_seq + t
-  if (blockIdx.y == 0 && threadIdx.x == 0) p.table[page] = page;
   if (!((p.live_bits[(size_t)b * p.words_per_seq + (t >> 5)] >> (t & 31)) & 1u)) return;
+  const int page = p.table[blockIdx.x];  // < capacity: the slot pass checked the count
   const bool is_v = blockIdx.y != 0;
   const uint8_t* src = static_cast<const uint8_t*>(is_v ? p.v_cache : p.k_cache);
   uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_out : p.k_out);
@@ -132,6 +164,9 @@ cudaError_t launch_fp8_dequant(const Fp8DequantParams& p, cudaStream_t stream) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  fp8_slots_kernel<<<1, kSlotThreads, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.num_seqs * p.tiles_per_seq), 2u);
   fp8_dequant_kernel<<<grid, kDequantThreads, 0, stream>>>(p);
   return cudaGetLastError();

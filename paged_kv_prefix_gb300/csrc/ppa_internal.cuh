@@ -132,6 +132,34 @@ __device__ __forceinline__ void tile_interval(int q_lo, int q_hi, int s, const M
   khi = hi;
 }
 
+// Scan across a block of 1024 threads (32 warps): returns the exclusive prefix of v and sets
+// *total to the block's sum. warp_sums: 32 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[31];
+  __syncthreads();
+  return before;
+}
+
 // Tile shape for a head group of G query heads: tq tokens x G heads <= 128 rows.
 __host__ __device__ constexpr int tokens_per_qtile(int group) { return kRowsPerTile / group; }
 __host__ __device__ constexpr int keys_per_tile(int) { return 128; }

@@ -103,7 +103,7 @@ cudaError_t launch_row_bounds(const MaskParams& mp, int num_seqs, int total_q, c
 // fp8 caches: the live cache key tiles of a planned batch, dequantised to bf16 scratch pages of
 // TN tokens (ppa_fp8_dequant.cu).
 struct Fp8DequantParams {
-  const WsHeader* ws;  // the plan's header (n_units)
+  WsHeader* ws;        // the plan's header (n_units; n_items cleared if the staging overflows)
   const Unit* units;
   int max_units;       // capacity of `units`
   const int32_t* context_lens;
@@ -112,15 +112,16 @@ struct Fp8DequantParams {
   const void* v_cache;
   const float* k_scale;
   const float* v_scale;
-  void* k_out;          // bf16 [num_seqs * tiles_per_seq][tn][Hkv][D]
+  void* k_out;          // bf16 [capacity][tn][Hkv][D]: the live tiles, packed
   void* v_out;
-  int32_t* table;       // identity block table [num_seqs * tiles_per_seq]
+  int32_t* table;       // [num_seqs][tiles_per_seq]: staging page of each live tile
   uint32_t* live_bits;  // [num_seqs][words_per_seq]
   int32_t* status;
   const int32_t* cu_query_lens;
   int kv_in_cache;  // cache positions run to c + n (new tokens already appended), not c
   int num_seqs, tiles_per_seq, words_per_seq, tn, page_size, num_pages, max_pages_per_seq;
   int row_codes;  // Hkv * D
+  int capacity;   // staging pages
 };
 cudaError_t launch_fp8_dequant(const Fp8DequantParams& p, cudaStream_t stream);
 

@@ -32,7 +32,7 @@ def test_status_strings_and_version():
     assert binding.ppa_status_string(0) == "ok"
     assert "timed out" in binding.ppa_status_string(binding.PPA_ERR_TIMEOUT)
     assert binding.ppa_status_string(99) == "unknown status"
-    assert binding.ppa_version() == 200  # the ppa_dims layout the binding mirrors
+    assert binding.ppa_version() == 300  # the ppa_dims layout the binding mirrors
 
 
 def _dims(**kw):
@@ -63,6 +63,32 @@ def test_fp8_workspace_holds_the_bf16_staging_unless_widened_in_kernel():
     assert staging <= binding.ppa_workspace_bytes(fp8) - base <= staging + 4 * 256 + 8 * tiles
 
 
+def test_auto_split_is_the_tuned_segment_length():
+    d = _dims(num_seqs=4, total_q=4, max_pages_per_seq=200, num_pages=900)
+    auto = binding.ppa_workspace_bytes(_dims(kv_split_tiles=-1, num_seqs=4, total_q=4,
+                                             max_pages_per_seq=200, num_pages=900))
+    tuned = binding.ppa_workspace_bytes(_dims(kv_split_tiles=32, num_seqs=4, total_q=4,
+                                              max_pages_per_seq=200, num_pages=900))
+    assert auto == tuned > binding.ppa_workspace_bytes(d)
+
+
+def test_fp8_staging_is_sized_by_the_cache_token_bound():
+    """max_cache_tokens > 0: floor(bound / 128) + 2 * num_seqs staging tiles, never more than
+    the block-table capacity; the table still covers every block-table slot."""
+    big = dict(kv_dtype=binding.PPA_KV_FP8_E4M3, num_seqs=32, total_q=70000, num_q_heads=32,
+               num_kv_heads=4, head_dim=128, page_size=544, max_pages_per_seq=61,
+               num_pages=2000)
+    full = binding.ppa_workspace_bytes(_dims(**big))
+    entries = 32 * -(-(61 * 544) // 128)
+    tile_bytes = 2 * 128 * 4 * 128 * 2  # K and V
+    for bound in (590_000, 131_072, 1):
+        got = binding.ppa_workspace_bytes(_dims(max_cache_tokens=bound, **big))
+        pages = min(entries, bound // 128 + 64)
+        assert full - got == (entries - pages) * tile_bytes
+    assert binding.ppa_workspace_bytes(_dims(max_cache_tokens=10**9, **big)) == full
+    assert binding.ppa_workspace_bytes(_dims(max_cache_tokens=-1, **big)) == 0
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 96, binding.PPA_ERR_UNSUPPORTED),
     ("num_kv_heads", 3, binding.PPA_ERR_INVALID),
@@ -76,6 +102,8 @@ def test_fp8_workspace_holds_the_bf16_staging_unless_widened_in_kernel():
     ("max_mm_ranges", -2, binding.PPA_ERR_INVALID),
     ("chunk_size", -1, binding.PPA_ERR_INVALID),
     ("kv_split_tiles", -3, binding.PPA_ERR_INVALID),
+    ("kv_split_tiles", -2, binding.PPA_ERR_INVALID),
+    ("max_cache_tokens", -1, binding.PPA_ERR_INVALID),
 ])
 def test_invalid_dims_rejected(field, value, code):
     d = _dims(**{field: value})
