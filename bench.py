@@ -83,7 +83,8 @@ def make_workload(name: str, seed: int):
     if name in ("decode", "decode_split"):
         return (f"decode: 32 seqs, ctx U[8192,32768], 1 new token each, 32 q / 8 kv heads, D 128, "
                 f"page 544, causal"
-                + (", split-KV in segments of 16 key tiles" if name == "decode_split" else ""),
+                + (", split-KV in the library's tuned segments (32 key tiles)"
+                   if name == "decode_split" else ""),
                 [wl.decode(seed=seed)])
     if name == "chunked":
         return ("chunked-local attention: 4 seqs x 32768 new tokens, 32 q / 8 kv heads, D 128, "
@@ -431,13 +432,16 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     binding.lib()
     desc, cases = make_workload(args.workload, seed=rank)
+    if args.split is not None:
+        desc += f"; kv_split_tiles {args.split}"
     if args.runs:  # a subset of the workload's runs (e.g. one launch for a profiler)
         keep = [int(x) for x in args.runs.split(",")]
         cases = [cases[i] for i in keep]
         desc += f"; runs {keep} only: " + ", ".join(c.name for c in cases)
     flags = workload_flags(args.workload)
     dcs = [binding.DeviceCase(c, device=dev, flags_extra=flags,
-                              kv_split_tiles=16 if args.workload == "decode_split" else 0,
+                              kv_split_tiles=(args.split if args.split is not None
+                                              else -1 if args.workload == "decode_split" else 0),
                               max_cache_tokens=cache_token_bound(c, flags))
            for c in cases]
     stream = torch.cuda.current_stream(dev)
@@ -813,6 +817,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed_serving")
+    ap.add_argument("--split", type=int, default=None,
+                    help="kv_split_tiles for every run (-1: the library's tuned length)")
     ap.add_argument("--runs", default="",
                     help="comma-separated indices: run only these runs (shapes) of the workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")

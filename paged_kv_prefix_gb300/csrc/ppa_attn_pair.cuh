@@ -199,7 +199,7 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
       const int s = kv_iter % ns;
       const uint32_t ph = (kv_iter / ns) & 1;
       // key position of this CTA's first row of the stage
-      const int key0 = kt * C::TN + (w == 0 ? static_cast<int>(sh.rank) * C::KH : 0);
+      const int key0 = kt * C::TN - u.koff + (w == 0 ? static_cast<int>(sh.rank) * C::KH : 0);
       // Classify this warp's 16-row chunks before waiting for the stage, so that the
       // block-table loads overlap the wait. Lane c < rpw/16 takes chunk c.
       int ctype = 0, crow = 0;  // 1 = cache box, 2 = new-token box, 0 = row gather
@@ -210,7 +210,7 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
             ctype = 2;
             crow = u.q_start + p0 - u.c;
           }
-        } else if (!FP8 && p0 + 15 < u.cs) {
+        } else if (!FP8 && p0 >= 0 && p0 + 15 < u.cs) {  // (chunks below key 0: zero fill)
           const int lp = p0 / p.page_size;
           if ((p0 + 15) / p.page_size == lp) {
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -258,7 +258,9 @@ __device__ void pair_producer(const AttnParams& p, const PairShared& sh, uint32_
         if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
           const char* mine = nullptr;
           const int pos = p_row0 + lane;
-          if (pos < u.cs) {
+          if (pos < 0) {
+            // below key 0 (a shifted first tile): zero fill
+          } else if (pos < u.cs) {
             const int lp = pos / p.page_size;
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
             if (page >= 0 && page < p.num_pages) {
@@ -509,7 +511,7 @@ __device__ void pair_softmax(const AttnParams& p, const PairShared& sh, uint32_t
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
       }
-      const int k0 = kt * C::TN;
+      const int k0 = kt * C::TN - u.koff;  // key position of the tile's first column
       const int a0 = kmin - k0, a1 = kmax - k0;  // allowed local columns [a0, a1]
       if (!(a0 <= 0 && a1 >= C::TN - 1)) {
 #pragma unroll

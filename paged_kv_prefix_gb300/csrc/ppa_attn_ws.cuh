@@ -172,6 +172,7 @@ struct UnitInfo {
   int b, g, t0, nt, c, n, s, q_start, lo, hi;
   int cs;  // key positions below cs come from the cache: c, or s when K/V are in the cache
   int part;  // split-KV segment: partial-result slot, -1 when the unit writes the output
+  int koff;  // key tile kt holds keys [kt * TN - koff, kt * TN - koff + TN)
   int lo_i[2], hi_i[2];
 };
 
@@ -189,6 +190,7 @@ __device__ __forceinline__ UnitInfo decode_item(const AttnParams& p, int item) {
   u.s = u.c + u.n;
   u.cs = p.kv_in_cache ? u.s : u.c;
   u.part = un.part;
+  u.koff = un.koff;
   u.lo_i[0] = un.lo0;
   u.hi_i[0] = un.hi0;
   u.lo_i[1] = un.nt > 1 ? un.lo1 : 0;
@@ -417,13 +419,13 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       // block-table loads overlap the wait. Lane c < RPW/16 takes chunk c.
       int ctype = 0, crow = 0;  // 1 = cache box, 2 = new-token box, 0 = row gather
       if (lane * 16 < RPW) {
-        const int p0 = kt * C::TN + half * RPW + 16 * lane;
+        const int p0 = kt * C::TN - u.koff + half * RPW + 16 * lane;
         if (p0 >= u.cs) {
           if (!p.kv_in_cache) {  // new tokens (cache-sourced: past the sequence, zero fill)
             ctype = 2;
             crow = u.q_start + p0 - u.c;
           }
-        } else if (!FP8 && p0 + 15 < u.cs) {
+        } else if (!FP8 && p0 >= 0 && p0 + 15 < u.cs) {  // (chunks below key 0: zero fill)
           const int lp = p0 / p.page_size;
           if ((p0 + 15) / p.page_size == lp) {
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -447,7 +449,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
         fp8_mask[sub] = 0;
         fp8_cache_rows[sub] = 0;
         const int row0 = half * RPW + 32 * sub;
-        const int p_row0 = kt * C::TN + row0;  // key position of this block's first row
+        const int p_row0 = kt * C::TN - u.koff + row0;  // key position of the block's first row
         int types[2], rows[2];
         uint32_t fb_mask = 0;
 #pragma unroll
@@ -479,7 +481,9 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
         if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
           const char* mine = nullptr;
           const int pos = p_row0 + lane;
-          if (pos < u.cs) {
+          if (pos < 0) {
+            // below key 0 (a shifted first tile): zero fill
+          } else if (pos < u.cs) {
             const int lp = pos / p.page_size;
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
             if (page >= 0 && page < p.num_pages) {
@@ -511,7 +515,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
         for (int sub = 0; sub < NSUB; ++sub) {
           if (sub == 0) cp_async_wait<1>(); else cp_async_wait<0>();
           if (fp8_mask[sub] != 0) {
-            if (kv_fold && u.cs >= (kt + 1) * C::TN)  // a cache-only tile: the softmax scales
+            if (kv_fold && u.cs >= (kt + 1) * C::TN - u.koff)  // cache-only: the softmax scales
               fp8_stage_widen<D, true>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub],
                                        sX, C::TN, stg + (32 * sub + lane) * D, kv_scale);
             else
@@ -787,7 +791,7 @@ __device__ void ws_softmax(const AttnParams& p, const WsShared& sh, uint32_t tme
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[cc * 64 + e] = __uint_as_float(r64[e]);
       }
-      const int k0 = kt * C::TN;
+      const int k0 = kt * C::TN - u.koff;  // key position of the tile's first column
       // fp8 with folded scales: a tile of cache keys only was widened without its scales.
       // The constants come from shared memory each tile (no registers held across tiles).
       float2 fc = make_float2(0.f, 0.f);  // (scale_log2 * k_scale * 2^112, log2(v_scale * 2^112))

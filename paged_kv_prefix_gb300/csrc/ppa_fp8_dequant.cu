@@ -36,14 +36,18 @@ __device__ __forceinline__ int cache_positions(const Fp8DequantParams& p, int b)
   return p.kv_in_cache ? c + (p.cu_query_lens[b + 1] - p.cu_query_lens[b]) : c;
 }
 
-// One thread per unit: marks the cache key tiles [lo, min(hi, ceil(cs / TN))) of its sequence
-// (cs: its cache positions), a word of 32 tiles per atomic.
+// One thread per unit: marks the cache tiles (TN-aligned, like the staging pages) that the
+// unit's key tiles overlap, up to ceil(cs / TN) (cs: the sequence's cache positions), a word
+// of 32 tiles per atomic. The unit's tiles lie on its shifted grid: keys [lo * TN - koff,
+// hi * TN - koff).
 __global__ void fp8_mark_kernel(Fp8DequantParams p) {
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= p.max_units || u >= p.ws->n_units) return;
   const Unit un = p.units[u];
-  const int lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
-  int hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
+  const int k_first = (un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0) * p.tn - un.koff;
+  const int k_end = (un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0) * p.tn - un.koff;
+  const int lo = k_first / p.tn;
+  int hi = (k_end + p.tn - 1) / p.tn;
   const int cs = cache_positions(p, un.seq);
   hi = min(hi, (cs + p.tn - 1) / p.tn);
   hi = min(hi, p.tiles_per_seq);

@@ -51,11 +51,21 @@ struct WsHeader {
 
 // One unit of work: nt (1 or 2) consecutive query tiles t0, t0+1 of sequence `seq` that
 // share one K/V stream, with each tile's live key tiles [lo_i, hi_i). `cost` is the number of
-// key tiles in the union.
+// key tiles in the union. The unit's key tiles lie on a grid shifted by `koff` keys: tile kt
+// holds keys [kt * TN - koff, kt * TN - koff + TN). The plan starts the grid at the 16-key
+// boundary at or below the unit's first live key, so a short window needs no more tiles than
+// its span (a 16-key chunk still lies in one page whenever the page size is a multiple of 16).
 struct Unit {
   int32_t seq, t0, nt, lo0, hi0, lo1, hi1, cost;
   int32_t part;  // split-KV segment: its partial-result slot (x Hkv + kv head); -1: not split
+  int32_t koff;  // key grid offset, 0 .. TN-16 in steps of 16
 };
+
+// Offset of the key-tile grid whose first tile starts at the 16-key boundary at or below kmin.
+__host__ __device__ __forceinline__ int key_grid_offset(int kmin, int tn) {
+  const int kb = kmin & ~15;
+  return (tn - kb % tn) % tn;
+}
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);

@@ -42,23 +42,36 @@ __device__ __forceinline__ int seq_query_len(const Stage1Params& p, int b, int* 
   return ok ? n : 0;
 }
 
-// Live key tiles of query tile t of a sequence (context c, n queries).
-__device__ __forceinline__ void qtile_bounds(const Stage1Params& p, int seq, int c, int n, int t,
-                                             int* lo, int* hi) {
+// Live keys [klo, khi] of query tile t of a sequence (context c, n queries); every key with
+// no_prune (testing) unless `pruned` asks for the live ones regardless.
+__device__ __forceinline__ void qtile_keys(const Stage1Params& p, int seq, int c, int n, int t,
+                                           int* klo, int* khi, bool pruned = false) {
   const int s = c + n;
-  if (p.no_prune) {
-    *lo = 0;
-    *hi = (s + p.tn - 1) / p.tn;
+  if (p.no_prune && !pruned) {
+    *klo = 0;
+    *khi = s - 1;
     return;
   }
   const int q_lo = c + t * p.tq;
   const int q_hi = c + min(n, (t + 1) * p.tq) - 1;
   const int32_t* ranges =
       p.mask.mm_ranges ? p.mask.mm_ranges + (size_t)seq * p.mask.max_mm_ranges * 2 : nullptr;
+  tile_interval(q_lo, q_hi, s, seq_mask(p.mask, seq), ranges, *klo, *khi);
+}
+
+// Live key tiles of query tile t of a sequence, on the grid aligned to multiples of tn.
+__device__ __forceinline__ void qtile_bounds(const Stage1Params& p, int seq, int c, int n, int t,
+                                             int* lo, int* hi) {
   int klo, khi;
-  tile_interval(q_lo, q_hi, s, seq_mask(p.mask, seq), ranges, klo, khi);
+  qtile_keys(p, seq, c, n, t, &klo, &khi);
   *lo = klo / p.tn;
   *hi = khi / p.tn + 1;
+}
+
+// Key tiles [lo, hi) covering keys [klo, khi] on the grid shifted by koff.
+__device__ __forceinline__ void grid_tiles(int klo, int khi, int koff, int tn, int* lo, int* hi) {
+  *lo = (klo + koff) / tn;
+  *hi = (khi + koff) / tn + 1;
 }
 
 // Last index r in [0, count) with base[r] <= x (base non-decreasing, base[0] <= x).
@@ -148,9 +161,11 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
       if (bad) atomicExch(&s_err, 1);
       const int nt = (n + p.tq - 1) / p.tq;
       nu = (nt + p.nq - 1) / p.nq;
-      if (p.split_tiles > 0 && nt == 1 && !bad) {
-        int lo, hi;
-        qtile_bounds(p, b, c, n, 0, &lo, &hi);
+      if (p.split_tiles > 0 && nt == 1 && !bad) {  // the tiles of step 2's single-tile unit
+        int klo, khi, plo, phi, lo, hi;
+        qtile_keys(p, b, c, n, 0, &klo, &khi);
+        qtile_keys(p, b, c, n, 0, &plo, &phi, true);
+        grid_tiles(klo, khi, key_grid_offset(plo, p.tn), p.tn, &lo, &hi);
         const int segs = (hi - lo + p.split_tiles - 1) / p.split_tiles;
         if (segs >= 2) nu = nseg = segs;
       }
@@ -196,8 +211,22 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
         p.seq_split_base != nullptr && p.seq_split_base[b + 1] > p.seq_split_base[b];
     const int t0 = split ? 0 : lu * p.nq;
     const int cnt = split ? 1 : min(p.nq, nt - t0);
-    Unit un{b, t0, cnt, 0, 0, 0, 0, 0, -1};
-    qtile_bounds(p, b, c, n, t0, &un.lo0, &un.hi0);
+    Unit un{b, t0, cnt, 0, 0, 0, 0, 0, -1, 0};
+    // The grid is the pruned unit's, also without pruning (testing): the tiles of the pruned
+    // run are then a subset of the unpruned run's, whose extra tiles are fully masked, and
+    // the two outputs agree bit for bit. Its first tile may then hold keys below 0, which
+    // the attention kernels read as zeros and mask.
+    int klo0, khi0, klo1 = 0, khi1 = 0, plo, phi;
+    qtile_keys(p, b, c, n, t0, &klo0, &khi0);
+    qtile_keys(p, b, c, n, t0, &plo, &phi, true);
+    if (cnt > 1) {
+      int plo1, phi1;
+      qtile_keys(p, b, c, n, t0 + 1, &klo1, &khi1);
+      qtile_keys(p, b, c, n, t0 + 1, &plo1, &phi1, true);
+      plo = min(plo, plo1);
+    }
+    un.koff = key_grid_offset(plo, p.tn);
+    grid_tiles(klo0, khi0, un.koff, p.tn, &un.lo0, &un.hi0);
     if (split) {  // segment lu of the tile's key tiles
       un.lo0 += lu * p.split_tiles;
       un.hi0 = min(un.hi0, un.lo0 + p.split_tiles);
@@ -205,7 +234,7 @@ __global__ void __launch_bounds__(kStage1Threads) plan_kernel(const Stage1Params
     }
     int lo = un.lo0, hi = un.hi0;
     if (cnt > 1) {
-      qtile_bounds(p, b, c, n, t0 + 1, &un.lo1, &un.hi1);
+      grid_tiles(klo1, khi1, un.koff, p.tn, &un.lo1, &un.hi1);
       lo = min(lo, un.lo1);
       hi = max(hi, un.hi1);
     }
