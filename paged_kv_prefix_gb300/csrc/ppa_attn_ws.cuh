@@ -615,6 +615,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
     if (item < 0) break;
     const UnitInfo u = decode_item(p, item);
     const int lo0 = u.lo_i[0], hi0 = u.hi_i[0], lo1 = u.lo_i[1], hi1 = u.hi_i[1];
+    uint32_t early = 0;  // tiles whose first S was issued ahead of their first key tile
     if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
     q_phase ^= 1;
     tc_fence_after();
@@ -669,10 +670,23 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       const uint32_t ph = (kv_iter / NS) & 1;
       // first key tile of a query tile: its S (the one S whose K the issuer waits for)
       for (int i = 0; i < u.nt && ok; ++i) {
-        if (kt != (i ? lo1 : lo0)) continue;
+        if (kt != (i ? lo1 : lo0) || ((early >> i) & 1u)) continue;
         if (!sh.wait(wsbar::K_FULL + 8 * s, ph)) { ok = false; break; }
         tc_fence_after();
         issue_s(i, s);
+      }
+      // A tile whose interval starts one key tile later (a window or range edge between the
+      // two query tiles): issue its first S now, so that its softmax overlaps the other tile's
+      // first one instead of following it.
+      if (kt == u.lo && u.nt == 2 && ok) {
+        for (int i = 0; i < 2 && ok; ++i) {
+          if ((i ? lo1 : lo0) != kt + 1) continue;
+          const uint32_t kv1 = kv_iter + 1;
+          if (!sh.wait(wsbar::K_FULL + 8 * (kv1 % NS), (kv1 / NS) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(i, kv1 % NS);
+          early |= 1u << i;
+        }
       }
       // every S that reads K(kt) has now been issued (in this or the previous iteration)
       tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));
