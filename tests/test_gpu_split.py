@@ -69,3 +69,20 @@ def test_split_kv_noncausal_verify_rows():
     """Non-causal rows see keys on both sides: every segment holds some of each row's keys."""
     case = _decode_batch(64, 2, 5, seed=6, causal=False, window_right=40)
     assert_close(_run(case, 3), ref.attention(case.numpy_inputs()), "split non-causal")
+
+
+def test_rejected_split_batch_writes_nothing_past_the_output():
+    """Lengths the plan rejects (a middle sequence runs past total_q) with split-KV on: the
+    device reports PPA_ERR_INVALID and neither the attention nor the merge writes a row, in
+    particular none past total_q (the output view is the head of a larger, sentinel-filled
+    buffer)."""
+    case = wl.build_case("bad_split", [300, 40, 20], [1, 1, 1], 2, 1, 128, 16, causal=True,
+                         seed=8)
+    dc = binding.DeviceCase(case, kv_split_tiles=2)
+    big = torch.full((case.total_q + 200, 2, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[: case.total_q]
+    dc.cu_query_lens.copy_(torch.tensor([0, 1, 100, 3], dtype=torch.int32))  # sequence 1: n = 99
+    dc.run(out=out)
+    torch.cuda.synchronize()
+    assert dc.read_status() == binding.PPA_ERR_INVALID
+    assert bool((big.float() == 7.0).all())
