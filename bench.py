@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload mixed_serving|mixed_serving_fp8|nonpow2|swa64|swa1024|mm|mixed|
                                 mixed_fp8|mixed_window|mixed_cached|chunked|decode|decode_split|
-                                decode_fp8|decode_fp8_inkernel]
+                                decode_fp8|decode_fp8_inkernel|mixed_fp8_inkernel]
                     [--no-cpu-baseline] [--sweep windows|pages|splits|groups]
 
 A step is one pass of the whole hot path over one batch: for every run (shape) of the
@@ -70,9 +70,11 @@ def make_workload(name: str, seed: int):
     if name == "mixed":
         return ("mixed serving: 32 seqs, ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, "
                 "D 128, causal, page 544, no window, bf16 KV", [wl.mixed(544, False, seed=seed)])
-    if name == "mixed_fp8":
+    if name in ("mixed_fp8", "mixed_fp8_inkernel"):
         return ("mixed serving, fp8 e4m3 KV cache (one per-tensor scale each for K and V): 32 seqs, "
-                "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544",
+                "ctx U[4096,32768], q U[512,4096], 32 q / 4 kv heads, D 128, causal, page 544"
+                + ("; e4m3 rows widened in the attention kernel" if name.endswith("inkernel")
+                   else ""),
                 [wl.mixed(544, False, kv_dtype="fp8_e4m3", seed=seed)])
     if name in ("decode_fp8", "decode_fp8_inkernel"):
         return ("decode over an fp8 e4m3 cache: 32 seqs, ctx U[8192,32768], 1 new token each, "
@@ -129,7 +131,7 @@ def workload_flags(name: str) -> int:
     from paged_kv_prefix_gb300 import binding
     if name == "mixed_cached":
         return binding.PPA_FLAG_KV_IN_CACHE
-    return binding.PPA_FLAG_FP8_INKERNEL if name == "decode_fp8_inkernel" else 0
+    return binding.PPA_FLAG_FP8_INKERNEL if name.endswith("_inkernel") else 0
 
 
 def cache_token_bound(case, flags: int) -> int:

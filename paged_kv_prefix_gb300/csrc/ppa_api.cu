@@ -188,6 +188,22 @@ bool encode_rows(CUtensorMap* m, const void* ptr, int head_dim, int heads, long 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An fp8 cache [rows][heads][D] as e4m3 bytes, seen as dims {D, heads, rows}, with a box of
+// {D, 1, 16} rows in the swizzle whose span is one row (128-byte rows at D 128, 64 at D 64): the
+// layout the attention kernel's staging area and its widening use.
+bool encode_rows_u8(CUtensorMap* m, const void* ptr, int head_dim, int heads, long long rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr || (head_dim != 64 && head_dim != 128)) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim, (cuuint64_t)heads * head_dim};
+  const cuuint32_t box[3] = {(cuuint32_t)head_dim, 1u, 16u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -370,6 +386,11 @@ ppa_status attend_impl(const ppa_dims* dims, const void* q, const void* k_new, c
               encode_rows(&a.tm.v_new, v_new, D, dims->num_kv_heads, dims->total_q, 1, 16) &&
               encode_rows(&a.tm.k_new32, k_new, D, dims->num_kv_heads, dims->total_q, 1, 32) &&
               encode_rows(&a.tm.v_new32, v_new, D, dims->num_kv_heads, dims->total_q, 1, 32);
+  if (maps_ok && fp8_kernel && D <= 128) {  // e4m3 rows boxed into the producers' staging
+    const long long cache_rows = (long long)a.num_pages * a.page_size;
+    maps_ok = encode_rows_u8(&a.tm.k_cache8, a.k_cache, D, dims->num_kv_heads, cache_rows) &&
+              encode_rows_u8(&a.tm.v_cache8, a.v_cache, D, dims->num_kv_heads, cache_rows);
+  }
   if (maps_ok && !fp8_kernel) {
     const long long cache_rows = (long long)a.num_pages * a.page_size;
     maps_ok = encode_rows(&a.tm.k_cache, a.k_cache, D, dims->num_kv_heads, cache_rows, 1, 16) &&

@@ -85,7 +85,8 @@ constexpr int ITEM_FULL = 0, ITEM_EMPTY = 16, Q_FULL = 32, Q_EMPTY = 40, K_FULL 
               V_FULL = 80, K_EMPTY = 112, S_FULL = 144, P_FULL = 160, O_DONE = 176,
               O_EMPTY = 192, FIN = 208, TMEM_SLOT = 216, ABORT = 220, RING = 224,
               V_EMPTY = 240, FOLD = 288,  // FOLD: fp8 scale constants, see Fp8Fold
-              LIMIT = 304;  // u64: ns before a wait gives up (read only once a wait is slow)
+              LIMIT = 304,  // u64: ns before a wait gives up (read only once a wait is slow)
+              STG_FULL = 312;  // [4] fp8: a producer warp's staging boxes landed
 constexpr int kRingConsumers = 14;  // warps 0..13 each release a ring slot once
 }  // namespace wsbar
 
@@ -265,6 +266,16 @@ __device__ __forceinline__ Fp8Fold fp8_fold(const AttnParams& p) {
   return f;
 }
 
+// Position of 16-byte piece `un` of staging row `row` (rows of D e4m3 codes). It is the layout
+// a TMA box lands in with the 128-byte swizzle (D 128: piece ^ row % 8) or the 64-byte one
+// (D 64: piece ^ (row / 2) % 4), so cp.async gathers and TMA boxes fill one staging area, and
+// the widening, which reads piece un of 32 rows at once, stays free of bank conflicts.
+template <int D>
+__device__ __forceinline__ int stg_piece(int un, int row) {
+  static_assert(D == 64 || D == 128, "staged e4m3 rows of 64 or 128 bytes");
+  return D == 128 ? ((un ^ row) & 7) : ((un ^ (row >> 1)) & 3);
+}
+
 // fp8 cache, first half of a 32-row block's gather (one row per lane): the lane copies its
 // row's raw e4m3 bytes (rows below `cache_rows`) into its staging row with cp.async, or its
 // bf16 new-token row straight into the stage. No registers hold the data, so all rows of the
@@ -276,11 +287,9 @@ __device__ __forceinline__ void fp8_stage_issue(const char* zero_src, int row0, 
   const int lane = threadIdx.x & 31;
   if (!((rowmask >> lane) & 1u)) return;
   if (lane < cache_rows) {
-    // 16-byte pieces at position un ^ (lane mod D/16): the widening reads stay free of bank
-    // conflicts although every lane's row starts at the same bank
 #pragma unroll
     for (int un = 0; un < D / 16; ++un)
-      cp_async_16(stg_row + ((un ^ lane) & (D / 16 - 1)) * 16, mine ? mine + un * 16 : zero_src,
+      cp_async_16(stg_row + stg_piece<D>(un, lane) * 16, mine ? mine + un * 16 : zero_src,
                   mine ? 16u : 0u);
   } else {
 #pragma unroll
@@ -302,7 +311,7 @@ __device__ __forceinline__ void fp8_stage_widen(int row0, uint32_t rowmask, int 
   const int row = row0 + lane;
 #pragma unroll
   for (int un = 0; un < D / 16; ++un) {
-    const uint4 codes = ld_shared_v4(stg_row + ((un ^ lane) & (D / 16 - 1)) * 16);
+    const uint4 codes = ld_shared_v4(stg_row + stg_piece<D>(un, lane) * 16);
     const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
     uint32_t v[8];
 #pragma unroll
@@ -387,6 +396,8 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const void* tm_cache = w == 0 ? (const void*)&p.tm.k_cache : (const void*)&p.tm.v_cache;
   const void* tm_new32 = w == 0 ? (const void*)&p.tm.k_new32 : (const void*)&p.tm.v_new32;
   const void* tm_cache32 = w == 0 ? (const void*)&p.tm.k_cache32 : (const void*)&p.tm.v_cache32;
+  // fp8: the cache as e4m3 bytes, boxes of 16 rows into this warp's staging area
+  const void* tm_cache8 = w == 0 ? (const void*)&p.tm.k_cache8 : (const void*)&p.tm.v_cache8;
   const char* g_cache = static_cast<const char*>(w == 0 ? p.k_cache : p.v_cache);
   const char* g_new = static_cast<const char*>(w == 0 ? p.k_new : p.v_new);
   if (lane == 0) {
@@ -397,6 +408,8 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
     if constexpr (!FP8) {
       tma_prefetch_desc(tm_cache);
       tma_prefetch_desc(tm_cache32);
+    } else {
+      tma_prefetch_desc(tm_cache8);
     }
   }
   const int empty_bar = w == 0 ? wsbar::K_EMPTY : wsbar::V_EMPTY;
@@ -404,6 +417,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
   const float kv_scale = FP8 ? *(w == 0 ? p.k_scale : p.v_scale) : 1.f;  // fp8 dequantisation
   const bool kv_fold = FP8 && fp8_fold(p).fold;
   uint32_t kv_iter = 0;
+  bool stg_pending = false;  // fp8: staging boxes of the current tile not yet seen landed
   for (int k = 0;; ++k) {
     const int item = ring_get(sh, k);
     if (item < 0) break;
@@ -425,7 +439,7 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
             ctype = 2;
             crow = u.q_start + p0 - u.c;
           }
-        } else if (!FP8 && p0 >= 0 && p0 + 15 < u.cs) {  // (chunks below key 0: zero fill)
+        } else if (p0 >= 0 && p0 + 15 < u.cs) {  // (chunks below key 0: zero fill)
           const int lp = p0 / p.page_size;
           if ((p0 + 15) / p.page_size == lp) {
             const int page = p.block_table[(size_t)u.b * p.max_pages_per_seq + lp];
@@ -439,11 +453,12 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
       if (!wait_warp(sh, empty_bar + 8 * s, ph ^ 1)) { ok = false; break; }
       const uint32_t sX = base + (w == 0 ? C::KV_OFF : C::V_OFF) + s * C::STAGE_STRIDE;
       const uint32_t bar = sh.bar(full_bar + 8 * s);
-      uint32_t bytes = 0;
+      uint32_t bytes = 0, stg_bytes = 0;
       bool any_fallback = false;
       uint32_t fp8_mask[NSUB];  // fp8: rows of each 32-row block still to widen
       int fp8_cache_rows[NSUB];
       const uint32_t stg = base + C::STG_OFF + pw * (C::STG_ROWS * D);  // this warp's staging
+      const uint32_t stg_bar = sh.bar(wsbar::STG_FULL + 8 * pw);
 #pragma unroll
       for (int sub = 0; sub < NSUB; ++sub) {
         fp8_mask[sub] = 0;
@@ -458,8 +473,10 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
           rows[c] = __shfl_sync(0xffffffffu, crow, 2 * sub + c);
           if (types[c] == 0) fb_mask |= 0xFFFFu << (16 * c);
         }
-        // both chunks from one contiguous source run: one 32-row box per column block
-        const bool one_run = types[0] != 0 && types[0] == types[1] && rows[1] == rows[0] + 16;
+        // both chunks from one contiguous source run: one 32-row box per column block (fp8
+        // cache chunks go to the staging area in boxes of their own instead)
+        const bool one_run = types[0] != 0 && types[0] == types[1] && rows[1] == rows[0] + 16 &&
+                             (!FP8 || types[0] == 2);
         if (lane == 0 && one_run) {
           const void* tm32 = types[0] == 1 ? tm_cache32 : tm_new32;
 #pragma unroll
@@ -471,12 +488,22 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             if (types[c] == 0) continue;
+            if (FP8 && types[c] == 1) {  // e4m3 rows into the staging, widened below
+              tma_load_3d(stg + (32 * sub + 16 * c) * D, tm_cache8, 0, u.g, rows[c], stg_bar);
+              stg_bytes += 16 * D;
+              continue;
+            }
 #pragma unroll
             for (int db = 0; db < D / 64; ++db)
               tma_load_3d(sX + db * (C::TN * 128) + (row0 + 16 * c) * 128,
                           types[c] == 1 ? tm_cache : tm_new, db * 64, u.g, rows[c], bar);
             bytes += (D / 64) * kChunkBytes;
           }
+        }
+        if constexpr (FP8) {  // the boxed cache rows are widened like the gathered ones
+          for (int c = 0; c < 2; ++c)
+            if (types[c] == 1) fp8_mask[sub] |= 0xFFFFu << (16 * c);
+          fp8_cache_rows[sub] = u.cs - p_row0;
         }
         if (fb_mask != 0) {  // row gather; lane r sources row row0 + r
           const char* mine = nullptr;
@@ -499,21 +526,25 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
           if constexpr (FP8) {
             fp8_stage_issue<D>(g_cache, row0, fb_mask, u.cs - p_row0, mine,
                                sX, C::TN, stg + (32 * sub + lane) * D);
-            fp8_mask[sub] = fb_mask;
-            fp8_cache_rows[sub] = u.cs - p_row0;
+            fp8_mask[sub] |= fb_mask;
           } else {
             gather_rows<D>(p, row0, 32, fb_mask, mine, sX);
           }
           any_fallback = true;
         }
-        if constexpr (FP8) cp_async_commit();  // one group per 32-row block
       }
       if constexpr (FP8) {
-        // widen block 0 while block 1's copies are still landing
-        static_assert(NSUB == 2, "two 32-row blocks per producer warp");
+        // every staged row has landed: the boxes (this warp's staging barrier, one phase per
+        // key tile) and the gathers
+        cp_async_commit();
+        if (lane == 0) mbar_arrive_expect_tx(stg_bar, stg_bytes);
+        stg_pending = true;
+        if (!wait_warp(sh, wsbar::STG_FULL + 8 * pw, kv_iter & 1)) { ok = false; break; }
+        stg_pending = false;
+        cp_async_wait<0>();
+        any_fallback = true;  // the widened rows are generic-proxy writes
 #pragma unroll
         for (int sub = 0; sub < NSUB; ++sub) {
-          if (sub == 0) cp_async_wait<1>(); else cp_async_wait<0>();
           if (fp8_mask[sub] != 0) {
             if (kv_fold && u.cs >= (kt + 1) * C::TN - u.koff)  // cache-only: the softmax scales
               fp8_stage_widen<D, true>(half * RPW + 32 * sub, fp8_mask[sub], fp8_cache_rows[sub],
@@ -538,6 +569,8 @@ __device__ void ws_producer(const AttnParams& p, const WsShared& sh, uint32_t ba
     if (!ok) break;
   }
   cp_async_wait<0>();
+  // staging boxes of a tile cut short by an abort (its phase: the current tile's)
+  if (FP8 && stg_pending && lane == 0) sh.drain(wsbar::STG_FULL + 8 * pw, kv_iter & 1);
   // This warp's TMA copies must land before the CTA exits: wait for the last fill of every
   // stage. After a normal end those fills are complete or complete shortly. After an abort a
   // fill whose other half was never issued cannot complete, and the wait gives up at the limit,
@@ -961,6 +994,8 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
       mbar_init(sh.bar(V_EMPTY + 8 * s), 1);
     }
     mbar_init(sh.bar(FIN), 1);
+    if constexpr (FP8)
+      for (int w = 0; w < 4; ++w) mbar_init(sh.bar(STG_FULL + 8 * w), 1);
     *sh.abort = 0;
     *reinterpret_cast<unsigned long long*>(barp + LIMIT) = p.wait_ns;
     if constexpr (FP8) {

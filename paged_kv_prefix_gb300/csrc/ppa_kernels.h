@@ -47,6 +47,9 @@ struct Stage1Params {
 struct TmaMaps {
   CUtensorMap q, k_new, v_new, k_cache, v_cache;
   CUtensorMap k_new32, v_new32, k_cache32, v_cache32;
+  // fp8 caches widened in the single-CTA kernel: [num_pages * P][Hkv][D] e4m3 bytes, boxes
+  // {D, 1, 16} with the 128-byte (D 128) or 64-byte (D 64) swizzle
+  CUtensorMap k_cache8, v_cache8;
 };
 
 struct AttnParams {
