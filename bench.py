@@ -124,7 +124,7 @@ def _launches_per_step(dc) -> int:
     live-tile marking, staging-slot and dequantisation kernels, plus the KV append, plus the
     split-KV merge."""
     return (2 + (3 if _prepass(dc) else 0) + (1 if _kv_in_cache(dc) else 0)
-            + (1 if dc.dims.kv_split_tiles > 0 else 0))
+            + (1 if dc.dims.kv_split_tiles != 0 else 0))
 
 
 def workload_flags(name: str) -> int:
@@ -537,7 +537,7 @@ def run_ours(args):
     roof["traffic"] = recorded_traffic(args.workload)
     roof["kernel"] = (f"{'fp8 dequant + ' if _prepass(dcs[dom]) else ''}"
                       f"{'attn_pair_kernel' if cases[dom].head_dim == 256 else 'attn_ws_kernel'}"
-                      f"{' + split merge' if dcs[dom].dims.kv_split_tiles > 0 else ''} "
+                      f"{' + split merge' if dcs[dom].dims.kv_split_tiles != 0 else ''} "
                       f"({cases[dom].name})")
     shapes = []
     for i, case in enumerate(cases):
