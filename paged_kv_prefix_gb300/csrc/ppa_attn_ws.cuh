@@ -3,8 +3,8 @@
 // One persistent CTA per SM, 16 warps:
 //   warps 0-3   softmax for query tile A (one thread per row)     \ 184 registers each
 //   warps 4-7   softmax for query tile B                          /
-//   warps 8-11  producers: TMA / cp.async paged K/V gather          \ 72 registers each
-//   warp  12    MMA issue (lane 0)                                  |
+//   warps 8-11  producers: TMA / cp.async paged K/V gather            56 registers each
+//   warp  12    MMA issue (lane 0)                                  \ 88 registers each
 //   warp  13    Q loads and the item ring                           |
 //   warps 14-15 idle                                               /
 // A unit of work is two consecutive 128-row query tiles (tq tokens x G heads each, token
@@ -621,6 +621,23 @@ __device__ void ws_qloader(const AttnParams& p, const WsShared& sh, uint32_t bas
   if (loaded && lane == 0) sh.drain(wsbar::Q_FULL, q_phase ^ 1);
 }
 
+// The tile intervals of a unit: the part of its decoding that the MMA issuer needs.
+struct UnitTiles {
+  int nt, lo, hi, lo_i[2], hi_i[2];
+};
+
+__device__ __forceinline__ UnitTiles unit_tiles(const Unit& un) {
+  UnitTiles t;
+  t.nt = un.nt;
+  t.lo_i[0] = un.lo0;
+  t.hi_i[0] = un.hi0;
+  t.lo_i[1] = un.nt > 1 ? un.lo1 : 0;
+  t.hi_i[1] = un.nt > 1 ? un.hi1 : 0;
+  t.lo = un.nt > 1 ? min(un.lo0, un.lo1) : un.lo0;
+  t.hi = un.nt > 1 ? max(un.hi0, un.hi1) : un.hi0;
+  return t;
+}
+
 // ---------------------------------------------------------------------------------------
 // MMA role (warp 12; lane 0 issues).
 // ---------------------------------------------------------------------------------------
@@ -643,10 +660,20 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
   // critical path between MMA batches.
   uint32_t kv_iter = 0, q_phase = 0, pf_bits = 0, oe_bits = 0;
   bool ok = true;
-  for (int k = 0; ok; ++k) {
-    const int item = ring_get1(sh, k);
-    if (item < 0) break;
-    const UnitInfo u = decode_item(p, item);
+  // The k-th item and its unit. The next one is taken once a unit's first S are issued (the
+  // issuer then waits for their softmax anyway), so its dependent loads are done when the
+  // unit ends and the next unit's first S follow its last PV without a gap.
+  int item = ring_get1(sh, 0);
+  Unit un_next{};
+  if (item >= 0) un_next = p.units[p.items[item] / p.num_kv_heads];
+  for (int k = 0; ok && item >= 0; ++k) {
+    const UnitTiles u = unit_tiles(un_next);
+    bool fetched = false;
+    auto fetch_next = [&]() {
+      item = ring_get1(sh, k + 1);
+      if (item >= 0) un_next = p.units[p.items[item] / p.num_kv_heads];
+      fetched = true;
+    };
     const int lo0 = u.lo_i[0], hi0 = u.hi_i[0], lo1 = u.lo_i[1], hi1 = u.hi_i[1];
     uint32_t early = 0;  // tiles whose first S was issued ahead of their first key tile
     if (!sh.wait(wsbar::Q_FULL, q_phase)) break;
@@ -723,6 +750,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       }
       // every S that reads K(kt) has now been issued (in this or the previous iteration)
       tc_commit(sh.bar(wsbar::K_EMPTY + 8 * s));
+      if (!fetched) fetch_next();
       // At the unit's last key tile every S has been issued: Q is free once they complete,
       // so the next unit's Q loads while this unit's last PVs and softmax run.
       if (kt == u.hi - 1) tc_commit(sh.bar(wsbar::Q_EMPTY));
@@ -751,6 +779,7 @@ __device__ void ws_mma(const AttnParams& p, const WsShared& sh, uint32_t base, u
       ++kv_iter;
       ++kt;
     }
+    if (ok && !fetched) fetch_next();  // (a unit without key tiles)
   }
 }
 
@@ -1021,7 +1050,14 @@ __global__ void __launch_bounds__(512, 1) attn_ws_kernel(const __grid_constant__
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
     ws_softmax<D, FP8, SPLIT>(p, sh, tmem);
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
+    // One count per warpgroup (setmaxnreg acts on whole warpgroups): the producers' (warps
+    // 8-11) 56, the MMA issuer's and query loader's warpgroup (12-15) 88, so that the issuer's
+    // state stays in registers. 256 x 184 + 128 x 56 + 128 x 88 = 512 x 128, the launch budget.
+    if (warp < 12) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    } else {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
+    }
     if (warp < 12) {
       ws_producer<D, FP8>(p, sh, base, n_items);
     } else if (warp == 13) {
