@@ -75,6 +75,9 @@ struct WsCfg {
   static constexpr int THREADS = 512;
   static_assert(TM_S + NQ * NSB * TN <= TMEM_COLS, "TMEM");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  // The barrier block holds four full and four empty barriers per stream (K_FULL, V_FULL,
+  // K_EMPTY and V_EMPTY, 8 bytes each): more stages would overlap the next array.
+  static_assert(NSK <= 4 && NSV <= 4, "stages per stream: at most the four barriers of each");
   static_assert(NQ == tiles_per_unit(D), "plan and kernel agree on query tiles per unit");
   static_assert(TN == keys_per_tile(D), "plan and kernel agree on the key tile");
 };
